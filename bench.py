@@ -1,0 +1,357 @@
+#!/usr/bin/env python3
+"""Benchmark: BN254 G1 multi-scalar multiplication on GB300.
+
+One step = one complete MSM (digits, sort, accumulation, bucket reduction,
+window combination) over seeded synthetic inputs already resident in HBM.
+Default workload: n = 2^16 points [r_i]G, uniform scalars, window c = 13,
+batch S = 8 (the pages' "logn=16" shape; PR #23520 "cache dx + idx in
+ba_fused_super pref_scratch", section "Measurements").  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Inputs fit in L2 (129 MB), so L2 is flushed (a 256 MiB write) before every
+timed step, outside the step's CUDA events.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per MSM and points/sec (BN254 G1, n=2^16..2^22); % of IMAD roofline"
+
+CONFIGS = {
+    "n2p10": dict(n=1 << 10, c=8, kind="uniform", seed=1001),
+    "n2p16": dict(n=1 << 16, c=13, kind="uniform", seed=1002),
+    "n2p20": dict(n=1 << 20, c=16, kind="uniform", seed=1003),
+    "n2p22": dict(n=1 << 22, c=16, kind="uniform", seed=1004),
+    "n2p20adv": dict(n=1 << 20, c=16, kind="adversarial", seed=1006),
+}
+
+# Pages' own figure for this metric and workload: Apple M2 (WebGPU, Chrome 148),
+# logn = 16, S = 8: 50.0 ms median MSM wall (PR #23738 "stream-walker S-sweep",
+# section "Real-hardware data").  Context only, another machine.
+PAGES_MS_LOGN16 = 50.0
+
+# Per-SM integer multiply-add lanes (4 sub-partitions x 16) of the sm_100
+# family; the IMAD roofline is SMs x 64 x SM clock.
+IMAD_PER_CLK_PER_SM = 64
+# 32-bit multiply instructions per Montgomery multiplication (CIOS, 8 limbs):
+# a_i * b lo/hi (2 * 64) + m * p lo/hi (2 * 64) + m = t0 * n' (8).
+IMAD_PER_FQ_MUL = 2 * 64 + 2 * 64 + 8
+FQ_MULS_PER_ADD = 6  # 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
+
+
+def fermat_inversion_muls():
+    """Field multiplications in the library's 4-bit fixed-window inversion of p - 2."""
+    p = 0x30644E72E131A029B85045B68181585D97816A916871CA8D3C208C16D87CFD47
+    nib = [int(ch, 16) for ch in "%064x" % (p - 2)]
+    first = next(i for i, v in enumerate(nib) if v)
+    sq = 4 * (len(nib) - 1 - first)
+    mul = sum(1 for v in nib[first + 1:] if v)
+    return 14 + sq + mul
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="n2p16", choices=sorted(CONFIGS))
+    ap.add_argument("--c", type=int, default=0, help="override the window size")
+    ap.add_argument("--batch-s", type=int, default=8)
+    ap.add_argument("--tpb", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(backend):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def workload(cfg):
+    from elliptic_curve_scalar_gb300 import synth
+    return synth.workload(cfg["kind"], cfg["n"], cfg["seed"])
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_points_per_s(cfg, sample, threads=None):
+    """Time the CPU oracle (as it stands) on the first ``sample`` terms."""
+    import oracle
+    r, k = workload(dict(cfg, n=sample))
+    pts = oracle.generator_multiples(r, threads=threads)
+    threads = threads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.msm(pts, k, threads=threads)
+    dt = time.perf_counter() - t0
+    return sample / dt, dt, threads
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_setup("gloo")
+    if rank != 0:
+        return 0
+    sample = 8192
+    vals, times = [], []
+    threads = None
+    for i in range(args.warmup + args.steps):
+        v, dt, threads = oracle_points_per_s(cfg, sample)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(dt)
+    value = sample * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "points/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u64", "data": "synthetic",
+        "config": {"workload": "BN254 G1 MSM %s, CPU oracle on the first %d terms per step" % (args.config, sample),
+                   "n": cfg["n"], "c": cfg["c"], "kind": cfg["kind"], "seed": cfg["seed"]},
+        "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
+                         "sample": "first %d terms of the %s workload per step" % (sample, args.config)},
+        "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.close()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+def run_gpu(args, cfg):
+    import torch
+    from elliptic_curve_scalar_gb300 import msm as gm
+    from elliptic_curve_scalar_gb300 import synth
+
+    world, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n = cfg["n"]
+    c = args.c or cfg["c"]
+    r, k = workload(cfg)
+
+    ctx = gm.MsmG1(n, c)
+    ctx.set_param(gm.PARAM_BATCH_S, args.batch_s)
+    ctx.set_param(gm.PARAM_TPB, args.tpb)
+    scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
+    # points P_i = [r_i]G built on the device by the library's fixed-base kernel
+    pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
+    out_d = torch.empty(24, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    pts_h = pts_d.cpu().pin_memory()
+    scal_h = scal_d.cpu().pin_memory()
+    out_h = torch.empty(24, dtype=torch.int32).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # warm-up (also fixes the launch count and the exact work counters)
+    ctx.set_param(gm.PARAM_STATS, 1)
+    for _ in range(max(args.warmup, 3)):
+        ctx.run(pts_d, scal_d, c, out=out_d)
+    stats = ctx.stats()
+    counts, _ = ctx.debug_read(0, gm.window_count(c) * (1 << (c - 1)))
+    ctx.set_param(gm.PARAM_STATS, 0)
+    ctx.set_param(gm.PARAM_TIMING, 1)
+    ctx.run(pts_d, scal_d, c, out=out_d)
+    ctx.phase_ms()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(uuid)
+    step_ms, phases = [], []
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()  # evict the inputs from L2 (outside the step's events)
+        starts[s].record(stream)
+        ctx.run(pts_d, scal_d, c, out=out_d)
+        ends[s].record(stream)
+        phases.append(ctx.phase_ms())  # waits for this step
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * n * args.steps / (total_ms / 1000.0)
+
+    # end to end through the public API with host buffers: H2D inputs from
+    # pinned memory, the MSM, D2H of the 96-byte result, every step
+    ctx.set_param(gm.PARAM_TIMING, 0)
+    e2e_steps = args.steps
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        p_in = pts_h.to(dev, non_blocking=True)
+        s_in = scal_h.to(dev, non_blocking=True)
+        ctx.run(p_in, s_in, c, out=out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # roofline of the dominant kernel: level-0 batched affine accumulation
+    m = counts.astype(np.int64)
+    adds_l0 = int((m // 2).sum())            # pairs with two operands at level 0
+    adds_total = int((m - (m > 0)).sum())    # every bucket of m entries needs m - 1 additions
+    l0_ms = statistics.mean(p["accum_l0"] for p in phases)
+    acc_ms = statistics.mean(p["accum_l0"] + p["accum_tree"] for p in phases)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    sm_max_mhz = peaks.get("sm_max_mhz", 2070.0)
+    peak_timad = sms * IMAD_PER_CLK_PER_SM * sm_max_mhz * 1e6 / 1e12
+    strict_imad = adds_l0 * FQ_MULS_PER_ADD * IMAD_PER_FQ_MUL
+    achieved = strict_imad / (l0_ms / 1e3) / 1e12
+    inv_muls = fermat_inversion_muls()
+    issued_imad = (adds_l0 * FQ_MULS_PER_ADD + adds_l0 / args.batch_s * inv_muls) * IMAD_PER_FQ_MUL
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tj = json.load(f)
+            key = "%s_S%d" % (args.config, args.batch_s)
+            traffic = tj.get(key)
+        except (OSError, ValueError):
+            traffic = None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = 32768
+        v, dt, threads = oracle_points_per_s(cfg, sample)
+        cpu = {"value": v, "unit": "points/s", "cores": threads, "kind": "oracle",
+               "sample": "first %d terms of the %s workload (%.1f s wall)" % (sample, args.config, dt)}
+
+    if rank == 0:
+        mean_phase = {kname: round(statistics.mean(p[kname] for p in phases), 4) for kname in phases[0]}
+        line = {
+            "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": (value / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) else None,
+            "dtype": "u32", "data": "synthetic",
+            "config": {"workload": "BN254 G1 MSM n=%d c=%d S=%d tpb=%d, %s points [r_i]G and scalars, seed %d"
+                                   % (n, c, args.batch_s, args.tpb, cfg["kind"], cfg["seed"]),
+                       "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"],
+                       "l2": "flushed before every timed step (256 MiB write)", "replicas": world},
+            "ms_per_msm": ms_per_step,
+            "ms_median": statistics.median(step_ms),
+            "phase_ms": mean_phase,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_timad, "unit": "TIMAD/s",
+                         "frac": achieved / peak_timad, "traffic": traffic,
+                         "kernel": "k_accum_level0",
+                         "peak_basis": "%d SMs x %d IMAD/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
+                                       % (sms, IMAD_PER_CLK_PER_SM, sm_max_mhz),
+                         "algorithmic_imad_per_launch": strict_imad,
+                         "adds_per_launch": adds_l0,
+                         "issued_frac_incl_inversion": issued_imad / (l0_ms / 1e3) / 1e12 / peak_timad,
+                         "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_PER_FQ_MUL
+                         / (acc_ms / 1e3) / 1e12 / peak_timad},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * n / (e2e_ms / 1e3), "unit": "points/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": int(pts_h.numel() * 4 + scal_h.numel() * 4),
+                    "d2h_bytes_per_step": 96},
+            "gpu_launches": int(stats.get("launches", 0)) * args.steps,
+            "clocks": clocks,
+            "work": {"entries": int(stats["entries"]), "adds": int(stats["adds"]),
+                     "inversions": int(stats["inversions"]), "levels": int(stats["levels"]),
+                     "max_bucket": int(stats["max_bucket"])},
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+// msm_core.cuh -- device building blocks shared by the MSM kernels and the
+// test hooks: scalar recoding and the batched affine pair addition.
+#pragma once
+#include <stdint.h>
+
+#include "fq.cuh"
+#include "g1.cuh"
+
+namespace msm {
+
+using fq::fe;
+using g1::aff;
+
+constexpr uint32_t HOLE = 0xFFFFFFFFu;  // padding entry: no second operand
+constexpr uint32_t SIGN = 0x80000000u;  // entry flag: negate the point
+
+// r = 0x30644e72e131a029b85045b68181585d2833e84879b9709143e1f593f0000001
+#define FR_R0 0xf0000001u
+#define FR_R1 0x43e1f593u
+#define FR_R2 0x79b97091u
+#define FR_R3 0x2833e848u
+#define FR_R4 0x8181585du
+#define FR_R5 0xb85045b6u
+#define FR_R6 0xe131a029u
+#define FR_R7 0x30644e72u
+
+__host__ __device__ constexpr int num_windows(int c) { return (255 + c - 1) / c; }
+
+// k := k mod r for any k < 2^256 (< 6r): subtract r while no borrow results.
+__device__ __forceinline__ void reduce_mod_r(uint32_t k[8]) {
+#pragma unroll 1
+    for (int it = 0; it < 5; it++) {
+        uint32_t d0, d1, d2, d3, d4, d5, d6, d7, br;
+        asm("sub.cc.u32  %0, %9,  %17;\n\t"
+            "subc.cc.u32 %1, %10, %18;\n\t"
+            "subc.cc.u32 %2, %11, %19;\n\t"
+            "subc.cc.u32 %3, %12, %20;\n\t"
+            "subc.cc.u32 %4, %13, %21;\n\t"
+            "subc.cc.u32 %5, %14, %22;\n\t"
+            "subc.cc.u32 %6, %15, %23;\n\t"
+            "subc.cc.u32 %7, %16, %24;\n\t"
+            "subc.u32    %8, 0, 0;"
+            : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3), "=r"(d4), "=r"(d5), "=r"(d6), "=r"(d7), "=r"(br)
+            : "r"(k[0]), "r"(k[1]), "r"(k[2]), "r"(k[3]), "r"(k[4]), "r"(k[5]), "r"(k[6]), "r"(k[7]),
+              "n"(FR_R0), "n"(FR_R1), "n"(FR_R2), "n"(FR_R3), "n"(FR_R4), "n"(FR_R5), "n"(FR_R6), "n"(FR_R7));
+        if (br) break;  // k < r
+        k[0] = d0; k[1] = d1; k[2] = d2; k[3] = d3; k[4] = d4; k[5] = d5; k[6] = d6; k[7] = d7;
+    }
+}
+
+__device__ __forceinline__ uint32_t limb_at(const uint32_t k[8], int i) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) r = (i == j) ? k[j] : r;
+    return r;
+}
+
+// c bits of k starting at bit o (bits past 255 read as zero)
+__device__ __forceinline__ uint32_t window_bits(const uint32_t k[8], int o, int c) {
+    int li = o >> 5;
+    uint64_t two = (uint64_t)limb_at(k, li) | ((uint64_t)limb_at(k, li + 1) << 32);
+    return (uint32_t)(two >> (o & 31)) & ((1u << c) - 1u);
+}
+
+// Signed digit of window w given the carry from window w-1: digits lie in
+// (-2^(c-1), 2^(c-1)]; a raw value above 2^(c-1) becomes raw - 2^c and carries
+// one into the next window.
+__device__ __forceinline__ int signed_digit(const uint32_t k[8], int w, int c, uint32_t& carry) {
+    uint32_t raw = window_bits(k, w * c, c) + carry;
+    uint32_t half = 1u << (c - 1);
+    if (raw > half) {
+        carry = 1;
+        return (int)raw - (int)(1u << c);
+    }
+    carry = 0;
+    return (int)raw;
+}
+
+__device__ __forceinline__ void load_scalar(const uint32_t* s, uint32_t k[8]) {
+    const uint4* q = reinterpret_cast<const uint4*>(s);
+    uint4 a = q[0], b = q[1];
+    k[0] = a.x; k[1] = a.y; k[2] = a.z; k[3] = a.w;
+    k[4] = b.x; k[5] = b.y; k[6] = b.z; k[7] = b.w;
+}
+
+// ---------------------------------------------------------------------------
+// Batched affine pair addition.
+//
+// A slot holds one pair (P, Q) and produces P + Q.  The denominator of the
+// chord (or tangent) slope is d = x_Q - x_P (d = 2 y_P when P = Q); S slots
+// share one inversion through Montgomery's trick: prefix products
+// pre_k = d_0 ... d_k on the way forward, one inversion of pre_{S-1}, and on
+// the way back d_k^-1 = inv * pre_{k-1}, inv := inv * d_k.  This is the batch
+// the pages' stream walker amortises the inversion over ("cost-per-add =
+// |inv| / S", PR #23736 "stream-walker -- amortize the field inversion via
+// large S + private pref_scratch", section "Goal & lever"); the prefix array is
+// their pref_scratch.  Exceptional pairs (a missing second operand, an infinite
+// operand, Q = -P) get d = 1 so they cannot poison the shared product -- the
+// page records the "affine-add /0" that a colliding x otherwise causes (same
+// page, section "Change (correct, landed)").
+enum PairCase : int { PC_ADD = 0, PC_DBL = 1, PC_COPY_P = 2, PC_COPY_Q = 3, PC_INF = 4, PC_NONE = 5 };
+
+// Decide the case from the x coordinates; y is only read when x_P == x_Q.
+template <class LoadY>
+__device__ __forceinline__ int pair_case(bool has_q, const fe& xp, const fe& xq, LoadY&& load_y, fe& yp_out) {
+    if (!has_q) return PC_COPY_P;
+    if (fq::is_zero(xp)) return PC_COPY_Q;
+    if (fq::is_zero(xq)) return PC_COPY_P;
+    if (!fq::eq(xp, xq)) return PC_ADD;
+    fe yp, yq;
+    load_y(yp, yq);
+    yp_out = yp;
+    return fq::eq(yp, yq) ? PC_DBL : PC_INF;
+}
+
+__device__ __forceinline__ fe pair_denominator(int cs, const fe& xp, const fe& xq, const fe& yp) {
+    if (cs == PC_ADD) return fq::sub(xq, xp);
+    if (cs == PC_DBL) return fq::dbl(yp);
+    return fq::one();
+}
+
+// P + Q given d^-1 for the pair's denominator
+__device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, const fe& dinv) {
+    if (cs == PC_COPY_P) return p;
+    if (cs == PC_COPY_Q) return q;
+    if (cs == PC_INF || cs == PC_NONE) return g1::aff_inf();
+    fe num, x2;
+    if (cs == PC_ADD) {
+        num = fq::sub(q.y, p.y);
+        x2 = q.x;
+    } else {  // tangent: 3 x^2 / 2y
+        fe xx = fq::sqr(p.x);
+        num = fq::add(fq::dbl(xx), xx);
+        x2 = p.x;
+    }
+    fe lam = fq::mul(num, dinv);
+    aff r;
+    r.x = fq::sub(fq::sub(fq::sqr(lam), p.x), x2);
+    r.y = fq::sub(fq::mul(lam, fq::sub(p.x, r.x)), p.y);
+    return r;
+}
+
+// Run one batch of up to S pair additions.  Src supplies, per slot k < count:
+//   bool has_q(k); fe xp(k), xq(k); void ys(k, fe& yp, fe& yq);
+//   aff p(k), q(k); void store(k, const aff&).
+// Returns the number of slots that were true additions (ADD or DBL).
+template <int S, class Src>
+__device__ __forceinline__ int batch_pairs(Src& src, int count) {
+    fe pre[S];
+    fe acc = fq::one();
+    int adds = 0;
+#pragma unroll
+    for (int k = 0; k < S; k++) {
+        fe d = fq::one();
+        if (k < count) {
+            bool hq = src.has_q(k);
+            fe xp = src.xp(k);
+            fe xq = hq ? src.xq(k) : fq::zero();
+            fe yp = fq::zero();
+            int cs = pair_case(hq, xp, xq, [&](fe& a, fe& b) { src.ys(k, a, b); }, yp);
+            d = pair_denominator(cs, xp, xq, yp);
+            adds += (cs == PC_ADD || cs == PC_DBL);
+        }
+        acc = (k == 0) ? d : fq::mul(acc, d);
+        pre[k] = acc;
+    }
+    fe inv = fq::inv_fermat(acc);
+#pragma unroll
+    for (int k = S - 1; k >= 0; k--) {
+        if (k < count) {
+            aff p = src.p(k);
+            bool hq = src.has_q(k);
+            aff q = hq ? src.q(k) : g1::aff_inf();
+            fe yp_unused = p.y;
+            int cs = pair_case(hq, p.x, q.x, [&](fe& a, fe& b) { a = p.y; b = q.y; }, yp_unused);
+            fe d = pair_denominator(cs, p.x, q.x, p.y);
+            fe dinv = (k > 0) ? fq::mul(inv, pre[k - 1]) : inv;
+            if (k > 0) inv = fq::mul(inv, d);
+            src.store(k, pair_result(cs, p, q, dinv));
+        }
+    }
+    return adds;
+}
+
+}  // namespace msm

@@ -1,0 +1,644 @@
+// msm_g1.cu -- the BN254 G1 bucket-method MSM on sm_103a and its C ABI.
+//
+// Pipeline per call (all on the caller's stream, no host synchronisation):
+//   1. digits+histogram: each scalar is reduced mod r and recoded into signed
+//      c-bit digits; every non-zero digit d of window w counts one entry for
+//      bucket g = w*B + |d| - 1 (B = 2^(c-1)).  The window size c is the knob
+//      the pages fix at 13 for n = 2^16 (PR #23520 "cache dx + idx in
+//      ba_fused_super pref_scratch", section "Measurements").
+//   2. scan: exclusive prefix of the bucket counts, each padded to even, into
+//      the bucket offsets (the pages' sorted_count_list, PR #23738
+//      "stream-walker S-sweep", section "What would actually win").
+//   3. scatter: a counting sort writes, per bucket, the point indices with a
+//      negate flag (the sorted_bucket_list of the same section); odd buckets
+//      get one padding entry.
+//   4. accumulation, level 0: entries (2u, 2u+1) form pair u; every pair is
+//      one affine addition, batched S per thread with one shared inversion.
+//   5. accumulation, levels l >= 1: the pair tree halves each bucket's items
+//      in place until every bucket holds one point, its bucket sum.  (This is
+//      the pages' other accumulator, the level-wise pair tree "ba_fused_super"
+//      of PR #23520, section "Summary", rather than their sequential stream
+//      walker: on a 152-SM part every level offers n*W/2^(l+1) independent
+//      additions, enough to fill the GPU, where a walker's per-thread streams
+//      would have to be cut into pieces shorter than a bucket.)
+//   6. bucket reduction: per window T_w = sum_b b * S_b by running sums over
+//      short chunks, then a per-window tree sum.
+//   7. window combination: Q = sum_w 2^(c w) T_w by Horner's rule.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "../../include/msm_g1.h"
+#include "msm_internal.cuh"
+
+using fq::fe;
+using g1::aff;
+using g1::jac;
+
+namespace msm {
+
+constexpr int SCAN_TPB = 256;
+constexpr int SCAN_ITEMS = 8;
+constexpr int SCAN_TILE = SCAN_TPB * SCAN_ITEMS;
+constexpr int REDUCE_TPB = 256;
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// exclusive block scan; blockDim.x multiple of 32 and <= 1024
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sm, uint32_t& total) {
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t inc = warp_incl_scan(v);
+    if (lane == 31) sm[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < nw ? sm[lane] : 0;
+        uint32_t wi = warp_incl_scan(w);
+        if (lane < nw) sm[lane] = wi - w;
+        if (lane == 31) sm[32] = wi;
+    }
+    __syncthreads();
+    uint32_t r = sm[warp] + inc - v;
+    total = sm[32];
+    __syncthreads();
+    return r;
+}
+
+// ------------------------------------------------------ 1. digits + histogram
+
+// One thread per scalar; all lanes of a warp walk the windows together so that
+// lanes hitting the same bucket can share one atomic.
+__global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, int W,
+                              uint32_t* __restrict__ counts) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    bool live = i < n;
+    uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (live) {
+        load_scalar(scalars + 8 * i, k);
+        reduce_mod_r(k);
+    }
+    const uint32_t B = 1u << (c - 1);
+    uint32_t carry = 0;
+    int lane = threadIdx.x & 31;
+    for (int w = 0; w < W; w++) {
+        int d = signed_digit(k, w, c, carry);
+        uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
+        uint32_t peers = __match_any_sync(0xffffffffu, g);
+        if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
+    }
+}
+
+// ---------------------------------------------------------------- 2. scan
+
+// per tile: sum of counts padded to even; also the statistics
+__global__ void k_scan_reduce(const uint32_t* __restrict__ counts, uint32_t nb, uint32_t* __restrict__ tile_sums,
+                              ctl_t* ctl) {
+    __shared__ uint32_t sm[33];
+    uint32_t base = blockIdx.x * SCAN_TILE;
+    uint32_t s = 0, mx = 0, ne = 0, ent = 0;
+#pragma unroll
+    for (int j = 0; j < SCAN_ITEMS; j++) {
+        uint32_t g = base + j * SCAN_TPB + threadIdx.x;
+        uint32_t m = g < nb ? counts[g] : 0;
+        s += m + (m & 1);
+        mx = max(mx, m);
+        ne += m != 0;
+        ent += m;
+    }
+    uint32_t tot;
+    block_excl_scan(s, sm, tot);
+    if (threadIdx.x == 0) tile_sums[blockIdx.x] = tot;
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    ne = __reduce_add_sync(0xffffffffu, ne);
+    ent = __reduce_add_sync(0xffffffffu, ent);
+    if ((threadIdx.x & 31) == 0) {
+        if (mx) atomicMax(&ctl->max_count, mx);
+        if (ne) atomicAdd(&ctl->nonempty, ne);
+        if (ent) atomicAdd(&ctl->entries, ent);
+    }
+}
+
+// single block: exclusive scan of the tile sums in place; total -> ctl
+__global__ void k_scan_tiles(uint32_t* __restrict__ tile_sums, uint32_t ntiles, ctl_t* ctl) {
+    __shared__ uint32_t sm[33];
+    uint32_t carry = 0;
+    for (uint32_t base = 0; base < ntiles; base += blockDim.x) {
+        uint32_t i = base + threadIdx.x;
+        uint32_t v = i < ntiles ? tile_sums[i] : 0;
+        uint32_t tot;
+        uint32_t ex = block_excl_scan(v, sm, tot);
+        if (i < ntiles) tile_sums[i] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) ctl->total = carry;
+}
+
+// per tile: offsets, scatter cursors and the padding entry of odd buckets
+__global__ void k_scan_apply(const uint32_t* __restrict__ counts, uint32_t nb, const uint32_t* __restrict__ tile_sums,
+                             uint32_t* __restrict__ offsets, uint32_t* __restrict__ cursor,
+                             uint32_t* __restrict__ entries, const ctl_t* __restrict__ ctl) {
+    __shared__ uint32_t sm[33];
+    uint32_t base = blockIdx.x * SCAN_TILE + threadIdx.x * SCAN_ITEMS;  // contiguous run per thread
+    uint32_t m[SCAN_ITEMS];
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < SCAN_ITEMS; j++) {
+        uint32_t g = base + j;
+        m[j] = g < nb ? counts[g] : 0;
+        s += m[j] + (m[j] & 1);
+    }
+    uint32_t tot;
+    uint32_t off = tile_sums[blockIdx.x] + block_excl_scan(s, sm, tot);
+#pragma unroll
+    for (int j = 0; j < SCAN_ITEMS; j++) {
+        uint32_t g = base + j;
+        if (g < nb) {
+            offsets[g] = off;
+            cursor[g] = off;
+            if (m[j] & 1) entries[off + m[j]] = HOLE;
+        }
+        off += m[j] + (m[j] & 1);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) offsets[nb] = ctl->total;
+}
+
+// ------------------------------------------------------------- 3. scatter
+
+__global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c, int W,
+                          uint32_t* __restrict__ cursor, uint32_t* __restrict__ entries) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    bool live = i < n;
+    uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (live) {
+        load_scalar(scalars + 8 * i, k);
+        reduce_mod_r(k);
+    }
+    const uint32_t B = 1u << (c - 1);
+    uint32_t carry = 0;
+    int lane = threadIdx.x & 31;
+    uint32_t lt_mask = (1u << lane) - 1u;
+    for (int w = 0; w < W; w++) {
+        int d = signed_digit(k, w, c, carry);
+        uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
+        uint32_t peers = __match_any_sync(0xffffffffu, g);
+        int leader = __ffs(peers) - 1;
+        uint32_t pos = 0;
+        if (g != HOLE && lane == leader) pos = atomicAdd(&cursor[g], (uint32_t)__popc(peers));
+        pos = __shfl_sync(0xffffffffu, pos, leader);
+        if (g != HOLE) entries[pos + __popc(peers & lt_mask)] = (uint32_t)i | (d < 0 ? SIGN : 0u);
+    }
+}
+
+// ---------------------------------------------------------- 6. reduction
+
+// One thread per chunk of L consecutive buckets of one window:
+// C_j = sum_{i<L} (jL + i + 1) S_{jL+i} via running sums from the top bucket.
+__global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ counts,
+                                const uint32_t* __restrict__ offsets, int W, uint32_t B, uint32_t L,
+                                uint32_t G, uint32_t* __restrict__ chunks) {
+    uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (uint32_t)W * G) return;
+    uint32_t w = t / G, j = t % G;
+    uint32_t b0 = j * L;
+    uint32_t b1 = min(b0 + L, B);
+    jac run = g1::jac_inf(), sum = g1::jac_inf();
+    for (uint32_t b = b1; b-- > b0;) {
+        uint32_t g = w * B + b;
+        if (counts[g]) run = g1::add_mixed(run, g1::load_aff(items + (size_t)(offsets[g] >> 1) * 16));
+        sum = g1::add(sum, run);
+    }
+    if (b0) sum = g1::add(sum, g1::mul_small(run, b0));
+    g1::store_jac(chunks + (size_t)t * 24, sum);
+}
+
+// One block per window: T_w = sum_j C_j (strided partial sums, then a tree).
+__global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* __restrict__ chunks, uint32_t G,
+                                                               uint32_t* __restrict__ wsums) {
+    __shared__ uint32_t sm[REDUCE_TPB * 24];
+    uint32_t w = blockIdx.x;
+    jac acc = g1::jac_inf();
+    for (uint32_t j = threadIdx.x; j < G; j += blockDim.x)
+        acc = g1::add(acc, g1::load_jac(chunks + ((size_t)w * G + j) * 24));
+    g1::store_jac(sm + threadIdx.x * 24, acc);
+    __syncthreads();
+    for (uint32_t s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            jac o = g1::load_jac(sm + (threadIdx.x + s) * 24);
+            acc = g1::add(acc, o);
+            g1::store_jac(sm + threadIdx.x * 24, acc);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) g1::store_jac(wsums + (size_t)w * 24, acc);
+}
+
+// ---------------------------------------------------------- 7. combination
+
+__global__ void k_combine(const uint32_t* __restrict__ wsums, int W, int c, uint32_t* __restrict__ out) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    jac q = g1::load_jac(wsums + (size_t)(W - 1) * 24);
+    for (int w = W - 2; w >= 0; w--) {
+        for (int i = 0; i < c; i++) q = g1::dbl(q);
+        q = g1::add(q, g1::load_jac(wsums + (size_t)w * 24));
+    }
+    g1::store_jac(out, q);
+}
+
+__global__ void k_write_inf(uint32_t* out) {
+    if (threadIdx.x == 0) g1::store_jac(out, g1::jac_inf());
+}
+
+// ------------------------------------------------------ generator multiples
+
+// table[j] = [2^j]G, affine Montgomery; one thread doubles, then all normalise
+__global__ void k_gen_table_jac(uint32_t* __restrict__ tj) {
+    if (threadIdx.x != 0) return;
+    jac g{fq::one(), fq::one(), fq::one()};
+    g.Y = fq::dbl(g.Y);  // (1, 2, 1) in Montgomery form
+    for (int j = 0; j < 256; j++) {
+        g1::store_jac(tj + j * 24, g);
+        g = g1::dbl(g);
+    }
+}
+
+__global__ void k_gen_table_norm(const uint32_t* __restrict__ tj, uint32_t* __restrict__ table) {
+    int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j < 256) g1::store_aff(table + j * 16, g1::to_aff(g1::load_jac(tj + j * 24)));
+}
+
+__global__ void k_mul_generator(const uint32_t* __restrict__ scalars, size_t n, const uint32_t* __restrict__ table,
+                                uint32_t* __restrict__ out) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    uint32_t k[8];
+    load_scalar(scalars + 8 * i, k);
+    jac acc = g1::jac_inf();
+    for (int j = 0; j < 256; j++)
+        if ((k[j >> 5] >> (j & 31)) & 1) acc = g1::add_mixed(acc, g1::load_aff(table + j * 16));
+    g1::store_aff(out + i * 16, g1::to_aff(acc));
+}
+
+}  // namespace msm
+
+// ============================================================== host side
+
+using namespace msm;
+
+static const int kPhases = 7;
+
+struct msm_g1_ctx {
+    int device;
+    size_t max_n;
+    int max_c;
+    uint64_t cap_entries;  // padded entries
+    uint64_t cap_buckets;  // W * B
+    uint64_t cap_chunks;   // W * G
+    size_t scratch_bytes;
+    char* scratch;
+    uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
+    ctl_t* ctl;
+    bool gen_ready;
+    int batch_s, tpb, timing, stats;
+    int last_launches;
+    cudaEvent_t ev[kPhases + 1];
+    bool events_made;
+    bool have_timing;
+    int last_levels;
+};
+
+static int window_count(int c) { return (255 + c - 1) / c; }
+static uint32_t reduce_chunk_len(uint32_t B) {
+    // L ~ sqrt(B / 512), a power of two, at least 4: balances the per-thread
+    // running-sum chain against the per-window tree
+    uint32_t L = 4;
+    while ((uint64_t)L * L * 512 < B) L <<= 1;
+    return std::min(L, B);
+}
+
+struct sizing {
+    uint64_t entries, buckets, chunks;
+};
+
+static sizing size_for(size_t max_n, int max_c) {
+    sizing s{0, 0, 0};
+    int cmin = std::min(max_c, 8);
+    s.entries = (uint64_t)max_n * window_count(cmin);
+    for (int c = 1; c <= max_c; c++) {
+        uint64_t B = 1ull << (c - 1);
+        uint64_t wb = (uint64_t)window_count(c) * B;
+        uint64_t wg = (uint64_t)window_count(c) * ((B + reduce_chunk_len((uint32_t)B) - 1) / reduce_chunk_len((uint32_t)B));
+        s.buckets = std::max(s.buckets, wb);
+        s.chunks = std::max(s.chunks, wg);
+    }
+    s.entries += s.buckets;  // one padding entry per bucket at most
+    s.entries += 2;
+    return s;
+}
+
+static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align_up(bytes);
+        return o;
+    };
+    size_t o_ctl = take(sizeof(ctl_t));
+    size_t o_counts = take(4 * s.buckets);
+    size_t o_offsets = take(4 * (s.buckets + 1));
+    size_t o_cursor = take(4 * s.buckets);
+    size_t o_tiles = take(4 * (s.buckets / SCAN_TILE + 2));
+    size_t o_entries = take(4 * s.entries);
+    size_t o_items = take((size_t)64 * ((s.entries + 1) / 2));
+    size_t o_chunks = take((size_t)96 * s.chunks);
+    size_t o_wsums = take((size_t)96 * 256);
+    size_t o_table = take((size_t)64 * 256);
+    size_t o_tj = take((size_t)96 * 256);
+    if (assign) {
+        c->ctl = (ctl_t*)(c->scratch + o_ctl);
+        c->counts = (uint32_t*)(c->scratch + o_counts);
+        c->offsets = (uint32_t*)(c->scratch + o_offsets);
+        c->cursor = (uint32_t*)(c->scratch + o_cursor);
+        c->tile_sums = (uint32_t*)(c->scratch + o_tiles);
+        c->entries = (uint32_t*)(c->scratch + o_entries);
+        c->items = (uint32_t*)(c->scratch + o_items);
+        c->chunks = (uint32_t*)(c->scratch + o_chunks);
+        c->wsums = (uint32_t*)(c->scratch + o_wsums);
+        c->gen_table = (uint32_t*)(c->scratch + o_table);
+        c->gen_tj = (uint32_t*)(c->scratch + o_tj);
+    }
+    return off;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+#define CK(call)                                  \
+    do {                                          \
+        if ((call) != cudaSuccess) return MSM_G1_ERR_CUDA; \
+    } while (0)
+
+extern "C" {
+
+int msm_g1_window_count(int c) {
+    if (c < 1 || c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    return window_count(c);
+}
+
+int msm_g1_auto_window(size_t n) {
+    if (n < 2) return 4;
+    double lg = 0;
+    while (((size_t)1 << (int)(lg + 1)) <= n && lg < 62) lg += 1;
+    int c = (int)(0.8 * lg + 0.5);
+    return std::max(4, std::min(18, c));
+}
+
+size_t msm_g1_scratch_bytes(size_t max_n, int max_c) {
+    if (max_n < 1 || max_c < 1 || max_c > MSM_G1_MAX_WINDOW) return 0;
+    return layout(nullptr, size_for(max_n, max_c), false);
+}
+
+const char* msm_g1_strerror(int code) {
+    switch (code) {
+        case MSM_G1_OK: return "ok";
+        case MSM_G1_ERR_INVALID_ARG: return "invalid argument";
+        case MSM_G1_ERR_CUDA: return "CUDA error";
+        case MSM_G1_ERR_CAPACITY: return "context capacity exceeded";
+        case MSM_G1_ERR_ALLOC: return "allocation failed";
+        case MSM_G1_ERR_NO_DEVICE: return "no usable CUDA device (compute capability 10.3 required)";
+        default: return "unknown error";
+    }
+}
+
+int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
+    if (!out) return MSM_G1_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (max_n < 1 || max_n > (1ull << 30) || max_c < 1 || max_c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    sizing s = size_for(max_n, max_c);
+    if (s.entries >= (1ull << 31)) return MSM_G1_ERR_INVALID_ARG;  // offsets are 32-bit
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MSM_G1_ERR_NO_DEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MSM_G1_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return MSM_G1_ERR_NO_DEVICE;
+    msm_g1_ctx* c = (msm_g1_ctx*)calloc(1, sizeof(msm_g1_ctx));
+    if (!c) return MSM_G1_ERR_ALLOC;
+    c->device = dev;
+    c->max_n = max_n;
+    c->max_c = max_c;
+    c->cap_entries = s.entries;
+    c->cap_buckets = s.buckets;
+    c->cap_chunks = s.chunks;
+    c->scratch_bytes = layout(nullptr, s, false);
+    if (cudaMalloc((void**)&c->scratch, c->scratch_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free(c);
+        return MSM_G1_ERR_ALLOC;
+    }
+    layout(c, s, true);
+    c->batch_s = 8;
+    c->tpb = 128;
+    c->timing = 0;
+    *out = c;
+    return MSM_G1_OK;
+}
+
+void msm_g1_destroy(msm_g1_ctx* c) {
+    if (!c) return;
+    cudaDeviceSynchronize();
+    if (c->events_made)
+        for (int i = 0; i <= kPhases; i++) cudaEventDestroy(c->ev[i]);
+    cudaFree(c->scratch);
+    free(c);
+}
+
+int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
+    if (!c) return MSM_G1_ERR_INVALID_ARG;
+    switch (key) {
+        case MSM_G1_PARAM_BATCH_S:
+            if (value != 1 && value != 2 && value != 4 && value != 8 && value != 16)
+                return MSM_G1_ERR_INVALID_ARG;
+            c->batch_s = value;
+            return MSM_G1_OK;
+        case MSM_G1_PARAM_TPB:
+            if (value != 64 && value != 128 && value != 256) return MSM_G1_ERR_INVALID_ARG;
+            c->tpb = value;
+            return MSM_G1_OK;
+        case MSM_G1_PARAM_TIMING:
+            if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
+            c->timing = value;
+            return MSM_G1_OK;
+        case MSM_G1_PARAM_STATS:
+            if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
+            c->stats = value;
+            return MSM_G1_OK;
+        default:
+            return MSM_G1_ERR_INVALID_ARG;
+    }
+}
+
+int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
+    if (!c || !value) return MSM_G1_ERR_INVALID_ARG;
+    switch (key) {
+        case MSM_G1_PARAM_BATCH_S: *value = c->batch_s; return MSM_G1_OK;
+        case MSM_G1_PARAM_TPB: *value = c->tpb; return MSM_G1_OK;
+        case MSM_G1_PARAM_TIMING: *value = c->timing; return MSM_G1_OK;
+        case MSM_G1_PARAM_STATS: *value = c->stats; return MSM_G1_OK;
+        default: return MSM_G1_ERR_INVALID_ARG;
+    }
+}
+
+}  // extern "C"
+
+extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
+                          uint32_t* out, cudaStream_t st) {
+    if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
+    if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
+    int cw = window_c == 0 ? std::min(msm_g1_auto_window(n), c->max_c) : window_c;
+    if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    if (cw > c->max_c || n > c->max_n) return MSM_G1_ERR_CAPACITY;
+    const int W = window_count(cw);
+    const uint32_t B = 1u << (cw - 1);
+    const uint32_t nb = (uint32_t)W * B;
+    const uint64_t entries_ub = (uint64_t)n * W + nb;
+    if ((uint64_t)n * W + nb + 2 > c->cap_entries || nb > c->cap_buckets) return MSM_G1_ERR_CAPACITY;
+    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
+    c->have_timing = false;
+    if (c->timing && !c->events_made) {
+        for (int i = 0; i <= kPhases; i++) CK(cudaEventCreate(&c->ev[i]));
+        c->events_made = true;
+    }
+    auto mark = [&](int i) {
+        if (c->timing) cudaEventRecord(c->ev[i], st);
+    };
+    if (n == 0) {
+        CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
+        k_write_inf<<<1, 32, 0, st>>>(out);
+        c->last_launches = 1;
+        return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+    }
+    const int stats = c->stats;
+    int launches = 0;
+    mark(0);
+    CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
+    CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
+    {
+        unsigned blocks = (unsigned)((n + 255) / 256);
+        k_digits_hist<<<blocks, 256, 0, st>>>(scalars, n, cw, W, c->counts);
+        launches++;
+    }
+    mark(1);
+    const uint32_t ntiles = (nb + SCAN_TILE - 1) / SCAN_TILE;
+    k_scan_reduce<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->ctl);
+    k_scan_tiles<<<1, 1024, 0, st>>>(c->tile_sums, ntiles, c->ctl);
+    k_scan_apply<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->offsets, c->cursor, c->entries, c->ctl);
+    launches += 3;
+    mark(2);
+    {
+        unsigned blocks = (unsigned)((n + 255) / 256);
+        k_scatter<<<blocks, 256, 0, st>>>(scalars, n, cw, W, c->cursor, c->entries);
+        launches++;
+    }
+    mark(3);
+    launch_accum_level0(c->batch_s, c->tpb, points, c->entries, c->items, c->ctl, (entries_ub + 1) / 2, stats, st);
+    launches++;
+    mark(4);
+    // levels while some bucket may still hold two items: 2^level < max bucket <= n
+    int levels = 0;
+    for (int level = 1; ((uint64_t)1 << level) < (uint64_t)n; level++) {
+        launch_accum_level(c->batch_s, c->tpb, c->items, c->offsets, nb, c->ctl, (entries_ub + 1) / 2, level, stats, st);
+        levels++;
+        launches++;
+    }
+    c->last_levels = levels;
+    mark(5);
+    const uint32_t L = reduce_chunk_len(B);
+    const uint32_t G = (B + L - 1) / L;
+    {
+        uint32_t threads = (uint32_t)W * G;
+        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, st>>>(c->items, c->counts, c->offsets, W, B, L, G, c->chunks);
+        k_reduce_windows<<<W, REDUCE_TPB, 0, st>>>(c->chunks, G, c->wsums);
+        launches += 2;
+    }
+    mark(6);
+    k_combine<<<1, 32, 0, st>>>(c->wsums, W, cw, out);
+    launches++;
+    c->last_launches = launches;
+    mark(7);
+    if (cudaGetLastError() != cudaSuccess) return MSM_G1_ERR_CUDA;
+    c->have_timing = c->timing != 0;
+    return MSM_G1_OK;
+}
+
+extern "C" int msm_g1_last_phase_ms(msm_g1_ctx* c, float* ms, int nphase) {
+    if (!c || !ms || nphase < 0) return MSM_G1_ERR_INVALID_ARG;
+    if (!c->have_timing) return 0;
+    CK(cudaEventSynchronize(c->ev[kPhases]));
+    int k = std::min(nphase, kPhases);
+    for (int i = 0; i < k; i++) CK(cudaEventElapsedTime(&ms[i], c->ev[i], c->ev[i + 1]));
+    return k;
+}
+
+extern "C" int msm_g1_last_stats(msm_g1_ctx* c, uint64_t* out, int nout) {
+    if (!c || !out || nout < 0) return MSM_G1_ERR_INVALID_ARG;
+    ctl_t h;
+    CK(cudaSetDevice(c->device));
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));
+    uint64_t v[7] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
+                     (uint64_t)c->last_launches};
+    int k = std::min(nout, 7);
+    for (int i = 0; i < k; i++) out[i] = v[i];
+    return k;
+}
+
+extern "C" int msm_g1_mul_generator(msm_g1_ctx* c, const uint32_t* scalars, size_t n, uint32_t* out,
+                                    cudaStream_t st) {
+    if (!c) return MSM_G1_ERR_INVALID_ARG;
+    if (n == 0) return MSM_G1_OK;
+    if (!scalars || !out || !aligned16(scalars) || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
+    CK(cudaSetDevice(c->device));
+    if (!c->gen_ready) {
+        k_gen_table_jac<<<1, 32, 0, st>>>(c->gen_tj);
+        k_gen_table_norm<<<2, 128, 0, st>>>(c->gen_tj, c->gen_table);
+        c->gen_ready = true;
+    }
+    k_mul_generator<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(scalars, n, c->gen_table, out);
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_debug_read(msm_g1_ctx* c, int which, void* dst, size_t max_bytes, size_t* bytes) {
+    if (!c || !dst || !bytes) return MSM_G1_ERR_INVALID_ARG;
+    CK(cudaSetDevice(c->device));
+    CK(cudaDeviceSynchronize());
+    ctl_t h;
+    CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));
+    (void)h;
+    const void* src = nullptr;
+    size_t sz = 0;
+    // sizes come from the last run's window: recover nb from the offsets buffer length is not
+    // stored, so the caller passes max_bytes and reads what it needs
+    switch (which) {
+        case 0: src = c->counts; sz = 4 * c->cap_buckets; break;
+        case 1: src = c->offsets; sz = 4 * (c->cap_buckets + 1); break;
+        case 2: src = c->entries; sz = 4 * (size_t)h.total; break;
+        default: return MSM_G1_ERR_INVALID_ARG;
+    }
+    *bytes = sz;
+    size_t k = std::min(sz, max_bytes);
+    if (k) CK(cudaMemcpy(dst, src, k, cudaMemcpyDeviceToHost));
+    return MSM_G1_OK;
+}

@@ -1,0 +1,132 @@
+// msm_testing.cu -- test hooks: single device primitives of the MSM path run
+// over arrays, so that each can be compared with the CPU oracle.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/msm_g1_testing.h"
+#include "msm_core.cuh"
+
+using fq::fe;
+using g1::aff;
+using g1::jac;
+
+namespace {
+
+__global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    fe x = fq::load(a + 8 * i);
+    fe r;
+    switch (op) {
+        case MSM_G1_TEST_FQ_MUL: r = fq::mul(x, fq::load(b + 8 * i)); break;
+        case MSM_G1_TEST_FQ_SQR: r = fq::sqr(x); break;
+        case MSM_G1_TEST_FQ_ADD: r = fq::add(x, fq::load(b + 8 * i)); break;
+        case MSM_G1_TEST_FQ_SUB: r = fq::sub(x, fq::load(b + 8 * i)); break;
+        case MSM_G1_TEST_FQ_NEG: r = fq::neg(x); break;
+        default: r = fq::inv_fermat(x); break;
+    }
+    fq::store(out + 8 * i, r);
+}
+
+__global__ void k_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    switch (op) {
+        case MSM_G1_TEST_JAC_DBL: g1::store_jac(out + 24 * i, g1::dbl(g1::load_jac(a + 24 * i))); break;
+        case MSM_G1_TEST_JAC_ADD:
+            g1::store_jac(out + 24 * i, g1::add(g1::load_jac(a + 24 * i), g1::load_jac(b + 24 * i)));
+            break;
+        case MSM_G1_TEST_JAC_MIXED:
+            g1::store_jac(out + 24 * i, g1::add_mixed(g1::load_jac(a + 24 * i), g1::load_aff(b + 16 * i)));
+            break;
+        default: g1::store_aff(out + 16 * i, g1::to_aff(g1::load_jac(a + 24 * i))); break;
+    }
+}
+
+template <int S>
+struct PairArraySrc {
+    const uint32_t *a, *b;
+    uint32_t* out;
+    size_t i0;
+    __device__ __forceinline__ bool has_q(int) const { return true; }
+    __device__ __forceinline__ fe xp(int k) const { return fq::load(a + 16 * (i0 + k)); }
+    __device__ __forceinline__ fe xq(int k) const { return fq::load(b + 16 * (i0 + k)); }
+    __device__ __forceinline__ void ys(int k, fe& ya, fe& yb) const {
+        ya = fq::load(a + 16 * (i0 + k) + 8);
+        yb = fq::load(b + 16 * (i0 + k) + 8);
+    }
+    __device__ __forceinline__ aff p(int k) const { return g1::load_aff(a + 16 * (i0 + k)); }
+    __device__ __forceinline__ aff q(int k) const { return g1::load_aff(b + 16 * (i0 + k)); }
+    __device__ __forceinline__ void store(int k, const aff& r) { g1::store_aff(out + 16 * (i0 + k), r); }
+};
+
+template <int S>
+__global__ void k_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+    size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    size_t i0 = t * S;
+    if (i0 >= n) return;
+    int count = (int)((n - i0) < (size_t)S ? (n - i0) : (size_t)S);
+    PairArraySrc<S> src{a, b, out, i0};
+    msm::batch_pairs<S>(src, count);
+}
+
+__global__ void k_test_digits(const uint32_t* scalars, size_t n, int c, int32_t* digits) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    uint32_t k[8];
+    msm::load_scalar(scalars + 8 * i, k);
+    msm::reduce_mod_r(k);
+    int W = msm::num_windows(c);
+    uint32_t carry = 0;
+    for (int w = 0; w < W; w++) digits[i * W + w] = msm::signed_digit(k, w, c, carry);
+}
+
+bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
+                              cudaStream_t st) {
+    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV) return MSM_G1_ERR_INVALID_ARG;
+    bool needs_b = op == MSM_G1_TEST_FQ_MUL || op == MSM_G1_TEST_FQ_ADD || op == MSM_G1_TEST_FQ_SUB;
+    if (n == 0) return MSM_G1_OK;
+    if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
+    k_test_fq<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
+                              cudaStream_t st) {
+    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_TO_AFFINE) return MSM_G1_ERR_INVALID_ARG;
+    bool needs_b = op == MSM_G1_TEST_JAC_ADD || op == MSM_G1_TEST_JAC_MIXED;
+    if (n == 0) return MSM_G1_OK;
+    if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
+    k_test_g1<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n, int batch_s,
+                                     cudaStream_t st) {
+    if (n == 0) return MSM_G1_OK;
+    if (!a || !b || !out || !a16(a) || !a16(b) || !a16(out)) return MSM_G1_ERR_INVALID_ARG;
+    size_t threads;
+    switch (batch_s) {
+#define CASE(S)                                                                                  \
+    case S:                                                                                      \
+        threads = (n + S - 1) / S;                                                               \
+        k_test_batch_add<S><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n);    \
+        break;
+        CASE(1) CASE(2) CASE(4) CASE(8) CASE(16)
+#undef CASE
+        default: return MSM_G1_ERR_INVALID_ARG;
+    }
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_test_digits(const uint32_t* scalars, size_t n, int c, int32_t* digits, cudaStream_t st) {
+    if (c < 1 || c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    if (n == 0) return MSM_G1_OK;
+    if (!scalars || !digits || !a16(scalars)) return MSM_G1_ERR_INVALID_ARG;
+    k_test_digits<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(scalars, n, c, digits);
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}

@@ -1,0 +1,122 @@
+/*
+ * msm_g1.h -- C ABI of libmsm_g1.so: BN254 G1 multi-scalar multiplication
+ * Q = sum_i k_i * P_i on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the bucket-method MSM whose GPU kernels the source pages
+ * tune: scalars are split into c-bit windows ("n=2^16, c=13", PR #23520
+ * "cache dx + idx in ba_fused_super pref_scratch", section "Measurements"),
+ * points are grouped by bucket (the sorted_bucket_list / sorted_count_list
+ * buffers of PR #23738 "stream-walker S-sweep", section "What would actually
+ * win"), bucket sums are built from batched affine additions that share one
+ * field inversion per batch of S additions (PR #23736 "stream-walker --
+ * amortize the field inversion via large S + private pref_scratch", section
+ * "Goal & lever"), and the result must equal an independent CPU computation of
+ * the same sum (PR #23736, section "Change (correct, landed)").  The curve is
+ * BN254 G1: y^2 = x^3 + 3 over F_p, p = 0x30644e72...d87cfd47, generator
+ * (1, 2), prime group order r = 0x30644e72...f0000001.
+ *
+ * Data layout (all device memory unless stated otherwise, little-endian
+ * 32-bit limbs, 16-byte aligned base pointers):
+ *   point, affine:   16 x uint32: x[8], y[8], each in Montgomery form
+ *                    (x * 2^256 mod p), fully reduced (< p).  (0, 0) is the
+ *                    point at infinity.  Inputs are not checked for being on
+ *                    the curve; an off-curve input gives an unspecified point
+ *                    (never a fault).
+ *   scalar:          8 x uint32, a plain (not Montgomery) integer < 2^256.
+ *                    Values >= r are allowed and act as k mod r, because every
+ *                    point of E(F_p) has order dividing r.
+ *   result, Jacobian: 24 x uint32: X[8], Y[8], Z[8] in Montgomery form,
+ *                    representing (X/Z^2, Y/Z^3); Z = 0 is infinity.
+ *
+ * Errors: every entry point returns 0 on success or a negative MSM_G1_ERR_*
+ * code; argument errors are detected on the host before any device work is
+ * queued.  Calls are asynchronous on the given stream unless stated otherwise;
+ * a context is not thread-safe (one run at a time per context).
+ */
+#ifndef MSM_G1_H
+#define MSM_G1_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSM_G1_OK 0
+#define MSM_G1_ERR_INVALID_ARG (-1) /* null pointer, misaligned pointer, c out of range, bad key */
+#define MSM_G1_ERR_CUDA (-2)        /* a CUDA call or kernel launch failed */
+#define MSM_G1_ERR_CAPACITY (-3)    /* n or c needs more scratch than the context holds */
+#define MSM_G1_ERR_ALLOC (-4)       /* device or host allocation failed at create */
+#define MSM_G1_ERR_NO_DEVICE (-5)   /* no CUDA device, or not compute capability 10.3 */
+
+#define MSM_G1_MAX_WINDOW 20
+
+/* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
+#define MSM_G1_PARAM_BATCH_S 1 /* additions sharing one inversion per thread: 1, 2, 4, 8, 16 (default 8) */
+#define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
+#define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
+#define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
+
+typedef struct msm_g1_ctx msm_g1_ctx;
+
+/* Create a context on the current CUDA device and allocate its device
+ * scratch (one allocation, owned by the context).  Scratch covers every run
+ * with n <= max_n and c <= max_c whose entry count n * ceil(255/c) is at most
+ * max_n * ceil(255/min(8, max_c)); msm_g1_scratch_bytes gives the size.
+ * max_c in [1, MSM_G1_MAX_WINDOW]; max_n in [1, 2^30].  Synchronous.
+ * Returns MSM_G1_ERR_NO_DEVICE without a usable GPU, MSM_G1_ERR_ALLOC when the
+ * allocation fails.  On error *ctx is set to NULL. */
+int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
+
+/* Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
+ * points_affine: device, n x 16 uint32 (layout above), read only.
+ * scalars: device, n x 8 uint32, read only.
+ * window_c: 1..max_c, or 0 to let the library choose (msm_g1_auto_window).
+ * stream: the CUDA stream all work is queued on (0 = legacy default stream).
+ * The caller owns inputs and output and must keep them alive until the stream
+ * reaches the end of this call; the context's scratch is reused by the next
+ * call.  n = 0 writes infinity.  No host synchronisation. */
+int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
+               int window_c, uint32_t *out_jacobian, cudaStream_t stream);
+
+/* out_i = [k_i]G for the generator G = (1, 2), as affine Montgomery points
+ * (n x 16 uint32, infinity as (0, 0)).  scalars: device, n x 8 uint32, any
+ * 256-bit value.  A utility for building workloads P_i = [r_i]G on the device;
+ * it is not part of the MSM.  Asynchronous on stream. */
+int msm_g1_mul_generator(msm_g1_ctx *ctx, const uint32_t *scalars, size_t n, uint32_t *out_points_affine,
+                         cudaStream_t stream);
+
+/* Release the context's scratch (synchronises the device first).  NULL is a no-op. */
+void msm_g1_destroy(msm_g1_ctx *ctx);
+
+/* Set / read a tunable (MSM_G1_PARAM_*).  Takes effect on the next run. */
+int msm_g1_set_param(msm_g1_ctx *ctx, int key, int value);
+int msm_g1_get_param(const msm_g1_ctx *ctx, int key, int *value);
+
+/* With MSM_G1_PARAM_TIMING = 1: wait for the last run and copy up to nphase
+ * phase durations in milliseconds (decompose+histogram, scan, scatter,
+ * accumulate level 0, accumulate levels >= 1, bucket reduction, window
+ * combination) into ms.  Returns the number of phases written. */
+int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
+
+/* Counters of the last run (waits for it): out[0] = bucket entries (non-zero
+ * digits), out[1] = non-empty buckets, out[2] = largest bucket; with
+ * MSM_G1_PARAM_STATS = 1 also out[3] = affine additions performed by the
+ * accumulation, out[4] = field inversions it performed, out[5] = tree levels
+ * that had work (zero otherwise); out[6] = kernels the last run launched.
+ * Returns the number of counters written (at most nout). */
+int msm_g1_last_stats(msm_g1_ctx *ctx, uint64_t *out, int nout);
+
+/* Host-only helpers (no device work). */
+int msm_g1_window_count(int c);                      /* ceil(255 / c): signed windows for scalars reduced mod r */
+int msm_g1_auto_window(size_t n);                    /* the window the library picks for window_c = 0 */
+size_t msm_g1_scratch_bytes(size_t max_n, int max_c); /* device bytes msm_g1_create allocates */
+const char *msm_g1_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSM_G1_H */

@@ -1,0 +1,63 @@
+/*
+ * msm_g1_testing.h -- test hooks of libmsm_g1.so.  They run single device
+ * primitives of the MSM path on arrays so that the tests can compare each
+ * primitive with the CPU oracle.  Not needed to compute an MSM.
+ *
+ * All pointers are device pointers (16-byte aligned), arrays of n elements,
+ * field elements as 8 x uint32 Montgomery limbs (< p), points as in msm_g1.h.
+ * Calls are asynchronous on stream; they return 0 or a negative MSM_G1_ERR_*.
+ */
+#ifndef MSM_G1_TESTING_H
+#define MSM_G1_TESTING_H
+
+#include "msm_g1.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Field operations in F_p (the Montgomery multiplication the pages call the
+ * "montgomery products", PR #23520, section "Why not split the inverse loop
+ * too?"; the inversion is the one batched affine addition amortises, PR #23736,
+ * section "Goal & lever"). */
+#define MSM_G1_TEST_FQ_MUL 0 /* out = a * b           */
+#define MSM_G1_TEST_FQ_SQR 1 /* out = a * a           */
+#define MSM_G1_TEST_FQ_ADD 2 /* out = a + b           */
+#define MSM_G1_TEST_FQ_SUB 3 /* out = a - b           */
+#define MSM_G1_TEST_FQ_NEG 4 /* out = -a              */
+#define MSM_G1_TEST_FQ_INV 5 /* out = a^-1 (0 -> 0)   */
+int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
+
+/* Point operations.  JAC_* take and return Jacobian points (24 uint32),
+ * MIXED adds a Jacobian a and an affine b, TO_AFFINE normalises a Jacobian a
+ * into an affine out (16 uint32). */
+#define MSM_G1_TEST_JAC_DBL 0
+#define MSM_G1_TEST_JAC_ADD 1
+#define MSM_G1_TEST_JAC_MIXED 2
+#define MSM_G1_TEST_TO_AFFINE 3
+int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
+
+/* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i
+ * for affine a, b (16 uint32 each), with one field inversion shared by each
+ * run of batch_s consecutive pairs (batch_s as MSM_G1_PARAM_BATCH_S).
+ * Equal, opposite and infinite operands are allowed. */
+int msm_g1_test_batch_add(const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, int batch_s,
+                          cudaStream_t stream);
+
+/* Signed window digits of n scalars (8 uint32 each) as the MSM forms them:
+ * digits (n x ceil(255/c) int32, window-major per scalar) with each digit in
+ * (-2^(c-1), 2^(c-1)] and sum_w digit_w 2^(c w) = k mod r. */
+int msm_g1_test_digits(const uint32_t *scalars, size_t n, int c, int32_t *digits, cudaStream_t stream);
+
+/* Copy an internal buffer of the last run to host memory (synchronises):
+ * which = 0: bucket counts (W*B uint32), 1: even-padded bucket offsets
+ * (W*B+1 uint32), 2: sorted entries (offset[W*B] uint32: point index with
+ * bit 31 = negate, 0xffffffff = padding).  *bytes receives the buffer size;
+ * at most max_bytes are copied. */
+int msm_g1_debug_read(msm_g1_ctx *ctx, int which, void *host_dst, size_t max_bytes, size_t *bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSM_G1_TESTING_H */

@@ -1,0 +1,102 @@
+"""The C-ABI library loads, exports every function include/*.h declares, and
+its host-side logic (argument checks, sizing helpers) works without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from elliptic_curve_scalar_gb300 import build as lib_build
+from elliptic_curve_scalar_gb300 import msm as gm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(msm_g1_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return gm.lib()
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for must in ("msm_g1_create", "msm_g1_run", "msm_g1_destroy"):
+        assert must in names
+    assert len(names) >= 15
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_symbol_exported(lib, name):
+    assert hasattr(lib, name), name
+
+
+def test_window_count(lib):
+    for c in range(1, 21):
+        assert lib.msm_g1_window_count(c) == -(-255 // c)
+    assert lib.msm_g1_window_count(0) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_window_count(21) == gm.ERR_INVALID_ARG
+
+
+def test_auto_window(lib):
+    assert lib.msm_g1_auto_window(1 << 10) == 8
+    assert lib.msm_g1_auto_window(1 << 16) == 13
+    assert lib.msm_g1_auto_window(1 << 20) == 16
+    for n in (1, 2, 1000, 1 << 30):
+        assert 4 <= lib.msm_g1_auto_window(n) <= 18
+
+
+def test_scratch_bytes(lib):
+    a = lib.msm_g1_scratch_bytes(1 << 16, 13)
+    b = lib.msm_g1_scratch_bytes(1 << 20, 13)
+    c = lib.msm_g1_scratch_bytes(1 << 20, 16)
+    assert 0 < a < b <= c
+    # entries (4 B) and level-1 items (32 B per entry) dominate: n * W(8) * 36 B
+    assert b >= (1 << 20) * 32 * 36
+    assert lib.msm_g1_scratch_bytes(0, 8) == 0
+    assert lib.msm_g1_scratch_bytes(16, 0) == 0
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert lib.msm_g1_strerror(code)
+
+
+def test_argument_checks_before_device_work(lib):
+    """Null contexts and bad sizes are rejected on the host."""
+    vp = ctypes.c_void_p
+    assert lib.msm_g1_create(None, 16, 8) == gm.ERR_INVALID_ARG
+    ctx = vp()
+    assert lib.msm_g1_create(ctypes.byref(ctx), 16, 0) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_create(ctypes.byref(ctx), 0, 8) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_create(ctypes.byref(ctx), 16, 21) == gm.ERR_INVALID_ARG
+    assert not ctx.value
+    assert lib.msm_g1_run(None, None, None, 0, 8, None, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_set_param(None, gm.PARAM_BATCH_S, 8) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_mul_generator(None, None, 0, None, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_test_fq(99, None, None, None, 1, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_test_batch_add(vp(16), vp(16), vp(16), 4, 3, None) == gm.ERR_INVALID_ARG
+    lib.msm_g1_destroy(None)
+
+
+def test_no_device_is_reported():
+    """Without a GB300 the library refuses to create a context (no CPU path)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    ctx = ctypes.c_void_p()
+    rc = gm.lib().msm_g1_create(ctypes.byref(ctx), 16, 8)
+    assert rc == gm.ERR_NO_DEVICE and not ctx.value
+    with pytest.raises(gm.MsmError):
+        gm.MsmG1(16, 8)

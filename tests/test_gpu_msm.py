@@ -1,0 +1,265 @@
+"""MSM parity: the CUDA path against the CPU oracle, bit-exact after both are
+normalised to canonical affine coordinates (the MSM has exactly one correct
+affine result, so bucket, sort and tie order cannot change it).
+
+Small and medium sizes are compared with oracle.msm directly; the full-size
+workloads (n = 2^20, 2^22) are compared with the closed form
+[sum_i k_i r_i mod r]G, which holds for any n because P_i = [r_i]G.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import pyref
+from elliptic_curve_scalar_gb300 import msm as gm
+from elliptic_curve_scalar_gb300 import synth
+from tests.gpu_helpers import gpu_points, gpu_scalars, normalise, points_from_r, ints_to_u32
+
+pytestmark = pytest.mark.gpu
+
+_ctx = {}
+
+
+def ctx(max_n, max_c):
+    key = (max_n, max_c)
+    if key not in _ctx:
+        _ctx[key] = gm.MsmG1(max_n, max_c)
+    return _ctx[key]
+
+
+def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=8, tpb=128):
+    n = k.shape[0]
+    cx = ctx(max_n or max(n, 1), max_c or max(c, 1))
+    cx.set_param(gm.PARAM_BATCH_S, batch_s)
+    cx.set_param(gm.PARAM_TPB, tpb)
+    out = cx.run(gpu_points(points_affine), gpu_scalars(k), c)
+    return normalise(out)
+
+
+def expect_oracle(points_affine, k):
+    return oracle.msm(points_affine, k)
+
+
+def test_config1_n1024_c8():
+    """n = 2^10, c = 8, uniform points [r_i]G and scalars (seed 1001)."""
+    r, k = synth.uniform_workload(1 << 10, 1001)
+    pts = points_from_r(r)
+    got = run_gpu(pts, k, 8)
+    assert np.array_equal(got, expect_oracle(pts, k))
+    assert np.array_equal(got, oracle.closed_form(r, k))
+    assert oracle.is_on_curve(got)
+
+
+@pytest.mark.parametrize("n,c", [(1, 4), (2, 3), (3, 8), (7, 5), (31, 6), (33, 7), (100, 9),
+                                 (257, 10), (1000, 11), (4097, 12)])
+def test_small_sizes(n, c):
+    r, k = synth.uniform_workload(n, 2000 + n)
+    pts = points_from_r(r)
+    assert np.array_equal(run_gpu(pts, k, c), expect_oracle(pts, k))
+
+
+@pytest.mark.parametrize("c", list(range(1, 21)))
+def test_every_window_size(c):
+    r, k = synth.uniform_workload(1500, 3000 + c)
+    pts = points_from_r(r)
+    assert np.array_equal(run_gpu(pts, k, c, max_n=1500, max_c=20), expect_oracle(pts, k))
+
+
+@pytest.fixture(scope="module")
+def mid_case():
+    r, k = synth.uniform_workload(20000, 4242)
+    pts = points_from_r(r)
+    return pts, k, expect_oracle(pts, k)
+
+
+@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("tpb", [64, 128, 256])
+def test_knobs(mid_case, batch_s, tpb):
+    """Every batch size S and block size gives the same result (the pages
+    verified each S separately because failures were S-specific: PR #23736,
+    section "Real-hardware results")."""
+    pts, k, expect = mid_case
+    assert np.array_equal(run_gpu(pts, k, 13, max_n=20000, max_c=13, batch_s=batch_s, tpb=tpb), expect)
+
+
+def test_empty_input():
+    cx = ctx(16, 8)
+    pts = torch.zeros((0, 16), dtype=torch.int32, device="cuda")
+    ks = torch.zeros((0, 8), dtype=torch.int32, device="cuda")
+    out = cx.run(pts, ks, 8)
+    assert oracle.words_to_point(normalise(out)) is None
+
+
+@pytest.mark.parametrize("kval", [0, 1, 2, 3, pyref.R - 1, pyref.R, pyref.R + 1, (1 << 256) - 1, 1 << 255])
+def test_single_term(kval):
+    pts = points_from_r(oracle.ints_to_limbs([987654321]))
+    k = oracle.ints_to_limbs([kval])
+    assert np.array_equal(run_gpu(pts, k, 8, max_n=16, max_c=8), expect_oracle(pts, k))
+
+
+def test_all_zero_scalars():
+    r, _ = synth.uniform_workload(300, 5)
+    pts = points_from_r(r)
+    k = np.zeros((300, 4), dtype=np.uint64)
+    assert oracle.words_to_point(run_gpu(pts, k, 8)) is None
+
+
+@pytest.mark.parametrize("n", [2, 3, 64, 1000])
+def test_same_point_same_digit(n):
+    """Every entry lands in one bucket with the same point: level 0 pairs are
+    all doublings, later levels add equal partial sums (doublings again)."""
+    pts = points_from_r(oracle.ints_to_limbs([31337] * n))
+    k = np.zeros((n, 4), dtype=np.uint64)
+    k[:, 0] = 1
+    got = run_gpu(pts, k, 8, max_n=1000, max_c=8)
+    assert oracle.words_to_point(got) == pyref.mul(31337 * n % pyref.R, pyref.G)
+
+
+def test_opposite_points_cancel():
+    r = [11 + i for i in range(200)] + [pyref.R - 11 - i for i in range(200)]
+    k = oracle.ints_to_limbs([5 + (i % 200) for i in range(400)])
+    pts = points_from_r(oracle.ints_to_limbs(r))
+    assert oracle.words_to_point(run_gpu(pts, k, 6)) is None
+
+
+def test_infinity_inputs():
+    r, k = synth.uniform_workload(500, 77)
+    pts = points_from_r(r)
+    pts[::7] = 0  # (0, 0) = infinity
+    assert np.array_equal(run_gpu(pts, k, 9), expect_oracle(pts, k))
+
+
+@pytest.mark.parametrize("scal", ["ones", "uniform"])
+def test_progression_points(scal):
+    """The pages' failing workload: points in arithmetic progression make
+    partial sums collide in x (PR #23736, section "Change (correct, landed)")."""
+    r, k = synth.progression_workload(3000, 9, scalars=scal)
+    pts = points_from_r(r)
+    assert np.array_equal(run_gpu(pts, k, 7), expect_oracle(pts, k))
+
+
+def test_adversarial_small():
+    r, k = synth.adversarial_workload(30000, 1005)
+    pts = points_from_r(r)
+    assert np.array_equal(run_gpu(pts, k, 12, max_n=30000, max_c=16), expect_oracle(pts, k))
+
+
+def test_deterministic_result():
+    r, k = synth.uniform_workload(5000, 8)
+    pts = points_from_r(r)
+    a = run_gpu(pts, k, 11)
+    b = run_gpu(pts, k, 11)
+    assert np.array_equal(a, b)
+
+
+def test_sort_structure():
+    """The sorted bucket list: every entry sits in the bucket of its digit,
+    with the right negate flag; odd buckets carry one padding entry."""
+    n, c = 3000, 9
+    r, k = synth.uniform_workload(n, 99)
+    pts = points_from_r(r)
+    cx = ctx(n, c)
+    cx.set_param(gm.PARAM_BATCH_S, 8)
+    torch.cuda.synchronize()
+    cx.run(gpu_points(pts), gpu_scalars(k), c)
+    W, B = gm.window_count(c), 1 << (c - 1)
+    counts, _ = cx.debug_read(0, W * B)
+    offsets, _ = cx.debug_read(1, W * B + 1)
+    total = int(offsets[-1])
+    entries, nbytes = cx.debug_read(2, total)
+    assert nbytes == 4 * total
+    digits = gm.to_host(gm.test_digits(gpu_scalars(k), c)).view(np.int32)
+    expect_count = np.zeros(W * B, dtype=np.int64)
+    for w in range(W):
+        d = digits[:, w]
+        nz = d != 0
+        np.add.at(expect_count, w * B + np.abs(d[nz]) - 1, 1)
+    assert np.array_equal(counts.astype(np.int64), expect_count)
+    for g in range(W * B):
+        m = int(counts[g])
+        o = int(offsets[g])
+        assert o % 2 == 0 and int(offsets[g + 1]) - o == m + (m & 1)
+        seg = entries[o:o + m]
+        w, b = divmod(g, B)
+        idx = seg & 0x7FFFFFFF
+        neg = (seg >> 31) == 1
+        dig = digits[idx, w]
+        assert np.all(np.abs(dig) == b + 1) and np.all((dig < 0) == neg)
+        assert len(set(idx.tolist())) == m
+        if m & 1:
+            assert entries[o + m] == 0xFFFFFFFF
+
+
+def test_capacity_and_argument_errors():
+    cx = ctx(100, 8)
+    r, k = synth.uniform_workload(101, 1)
+    pts, ks = gpu_points(points_from_r(r)), gpu_scalars(k)
+    with pytest.raises(gm.MsmError) as e:
+        cx.run(pts, ks, 8)
+    assert e.value.code == gm.ERR_CAPACITY
+    with pytest.raises(gm.MsmError) as e:
+        cx.run(pts[:100], ks[:100], 9)
+    assert e.value.code == gm.ERR_CAPACITY
+    with pytest.raises(gm.MsmError) as e:
+        cx.run(pts[:100], ks[:100], 21)
+    assert e.value.code == gm.ERR_INVALID_ARG
+    flat = ks.reshape(-1)[1:8 * 50 + 1].reshape(50, 8)  # 4-byte offset: misaligned
+    with pytest.raises(gm.MsmError) as e:
+        cx.run(pts[:50], flat, 8)
+    assert e.value.code == gm.ERR_INVALID_ARG
+
+
+def test_mul_generator():
+    ks = [0, 1, 2, pyref.R - 1, pyref.R, (1 << 256) - 1] + synth.limbs_to_ints(synth.uniform_workload(3000, 6)[0])
+    kl = oracle.ints_to_limbs(ks)
+    cx = ctx(16, 8)
+    out = cx.mul_generator(gm.to_device(synth.scalars_to_u32(kl)))
+    torch.cuda.synchronize()
+    got = gm.to_host(out)
+    expect = oracle.points_to_gpu_layout(oracle.generator_multiples(kl))
+    assert np.array_equal(got, expect)
+
+
+# ------------------------------------------------------------ full sizes
+
+@pytest.fixture(scope="module")
+def big_points():
+    """2^22 uniform points [r_i]G from the oracle (prefixes serve 2^16, 2^20)."""
+    r, _ = synth.uniform_workload(1 << 22, 1004)
+    return r, points_from_r(r)
+
+
+def test_config2_n65536_c13(big_points):
+    r_all, pts_all = big_points
+    n = 1 << 16
+    _, k = synth.uniform_workload(n, 1002)
+    r, pts = r_all[:n], pts_all[:n]
+    got = run_gpu(pts, k, 13, max_n=n, max_c=13)
+    assert np.array_equal(got, expect_oracle(pts, k))
+    assert np.array_equal(got, oracle.closed_form(r, k))
+
+
+@pytest.mark.parametrize("batch_s", [4, 8, 16])
+def test_config3_n2p20_c16(big_points, batch_s):
+    r_all, pts_all = big_points
+    n = 1 << 20
+    _, k = synth.uniform_workload(n, 1003)
+    got = run_gpu(pts_all[:n], k, 16, max_n=n, max_c=16, batch_s=batch_s)
+    assert np.array_equal(got, oracle.closed_form(r_all[:n], k))
+
+
+@pytest.mark.parametrize("c", [16, 17, 18])
+def test_config4_n2p22(big_points, c):
+    r, pts = big_points
+    _, k = synth.uniform_workload(1 << 22, 1005)
+    got = run_gpu(pts, k, c, max_n=1 << 22, max_c=18)
+    assert np.array_equal(got, oracle.closed_form(r, k))
+
+
+def test_config5_adversarial_n2p20():
+    n = 1 << 20
+    r, k = synth.adversarial_workload(n, 1006)
+    pts = points_from_r(r)
+    got = run_gpu(pts, k, 16, max_n=n, max_c=16)
+    assert np.array_equal(got, oracle.closed_form(r, k))

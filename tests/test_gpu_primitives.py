@@ -1,0 +1,117 @@
+"""Device primitives (field, curve, batched affine addition, digit recoding)
+against the oracle's arithmetic (Python integers and the affine law of
+oracle.pyref), element by element and bit-exact."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import pyref
+from elliptic_curve_scalar_gb300 import msm as gm
+from tests.gpu_helpers import (P, R, mont, unmont, ints_to_u32, u32_to_ints, point_to_aff_words,
+                               aff_words_to_point, point_to_jac_words, jac_words_to_point)
+
+pytestmark = pytest.mark.gpu
+
+EDGE = [0, 1, 2, P - 1, P - 2, (1 << 255) % P, (1 << 128) - 1, (1 << 224), P >> 1, (1 << 254) % P]
+
+
+def _field_inputs(n, seed):
+    rng = random.Random(seed)
+    vals = EDGE + [rng.randrange(P) for _ in range(n - len(EDGE))]
+    return vals
+
+
+@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv"])
+def test_fq_ops(op):
+    n = 4099  # several blocks and a ragged tail
+    a = _field_inputs(n, 1)
+    b = list(reversed(_field_inputs(n, 2)))
+    da = gm.to_device(ints_to_u32([mont(x) for x in a]))
+    db = gm.to_device(ints_to_u32([mont(x) for x in b]))
+    out = gm.test_fq(op, da, db if op in ("mul", "add", "sub") else None)
+    got = [unmont(v) for v in u32_to_ints(gm.to_host(out))]
+    raw = u32_to_ints(gm.to_host(out))
+    assert all(v < P for v in raw), "result not fully reduced"
+    for x, y, g in zip(a, b, got):
+        if op == "mul":
+            e = x * y % P
+        elif op == "sqr":
+            e = x * x % P
+        elif op == "add":
+            e = (x + y) % P
+        elif op == "sub":
+            e = (x - y) % P
+        elif op == "neg":
+            e = (-x) % P
+        else:
+            e = pow(x, P - 2, P)
+        assert g == e, (op, x, y)
+
+
+def _rand_points(rng, n):
+    return [pyref.mul(rng.randrange(1, R), pyref.G) for _ in range(n)]
+
+
+def test_jacobian_ops():
+    rng = random.Random(5)
+    pts = _rand_points(rng, 40)
+    a = pts[:20] + [None, pts[0], pts[1], pts[2]]
+    b = pts[20:] + [pts[3], None, pts[1], pyref.neg(pts[2])]
+    zs = [rng.randrange(2, P) for _ in a]
+    ja = np.stack([point_to_jac_words(p, z) for p, z in zip(a, zs)])
+    jb = np.stack([point_to_jac_words(p, z + 7) for p, z in zip(b, zs)])
+    ab = np.stack([point_to_aff_words(p) for p in b])
+    da, db, dab = gm.to_device(ja), gm.to_device(jb), gm.to_device(ab)
+    dbl = gm.to_host(gm.test_g1("jac_dbl", da))
+    add = gm.to_host(gm.test_g1("jac_add", da, db))
+    mix = gm.to_host(gm.test_g1("jac_mixed", da, dab))
+    aff = gm.to_host(gm.test_g1("to_affine", da))
+    for i, (p, q) in enumerate(zip(a, b)):
+        assert jac_words_to_point(dbl[i]) == pyref.add(p, p), ("dbl", i)
+        assert jac_words_to_point(add[i]) == pyref.add(p, q), ("add", i)
+        assert jac_words_to_point(mix[i]) == pyref.add(p, q), ("mixed", i)
+        assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
+
+
+@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16])
+def test_batch_affine_add(batch_s):
+    """Batched affine pair additions, including pairs that would poison a
+    shared inversion: equal points (tangent), opposite points, infinity."""
+    rng = random.Random(100 + batch_s)
+    pts = _rand_points(rng, 60)
+    a, b = [], []
+    for i in range(37):
+        kind = i % 6
+        p, q = pts[i], pts[i + 20]
+        if kind == 1:
+            q = p                 # doubling
+        elif kind == 2:
+            q = pyref.neg(p)      # P + (-P) = infinity
+        elif kind == 3:
+            p = None              # infinity + Q
+        elif kind == 4:
+            q = None              # P + infinity
+        a.append(p)
+        b.append(q)
+    da = gm.to_device(np.stack([point_to_aff_words(p) for p in a]))
+    db = gm.to_device(np.stack([point_to_aff_words(p) for p in b]))
+    out = gm.to_host(gm.test_batch_add(da, db, batch_s))
+    for i, (p, q) in enumerate(zip(a, b)):
+        assert aff_words_to_point(out[i]) == pyref.add(p, q), (batch_s, i)
+
+
+@pytest.mark.parametrize("c", [1, 2, 5, 8, 13, 16, 17, 18, 20])
+def test_signed_digits(c):
+    rng = random.Random(c)
+    ks = [0, 1, R - 1, R, R + 1, (1 << 256) - 1, (1 << 254), 2 ** (c - 1), 2 ** c - 1]
+    ks += [rng.randrange(0, 1 << 256) for _ in range(300)]
+    d = gm.test_digits(gm.to_device(ints_to_u32(ks)), c)
+    digits = gm.to_host(d).view(np.int32)
+    W = gm.window_count(c)
+    assert digits.shape == (len(ks), W)
+    half = 1 << (c - 1)
+    for k, row in zip(ks, digits):
+        assert all(-half < int(v) <= half for v in row)
+        assert sum(int(v) << (c * w) for w, v in enumerate(row)) == k % R
