@@ -42,23 +42,15 @@ CONFIGS = {
 # section "Real-hardware data").  Context only, another machine.
 PAGES_MS_LOGN16 = 50.0
 
-# Per-SM integer multiply-add lanes (4 sub-partitions x 16) of the sm_100
-# family; the IMAD roofline is SMs x 64 x SM clock.
-IMAD_PER_CLK_PER_SM = 64
-# 32-bit multiply instructions per Montgomery multiplication (CIOS, 8 limbs):
-# a_i * b lo/hi (2 * 64) + m * p lo/hi (2 * 64) + m = t0 * n' (8).
-IMAD_PER_FQ_MUL = 2 * 64 + 2 * 64 + 8
+# IMAD roofline.  Each SM issues 64 low-half 32-bit multiply-adds per clock
+# (4 sub-partitions x 16 lanes) and the high-half form at half that rate
+# (measured on this GB300: mad.lo 18.7 Tops/s, mad.hi 8.7 Tops/s).  A
+# Montgomery multiplication on 8 x 32-bit limbs issues 64 + 64 low products
+# (a_i b_j, m_i p_j), 8 low products m_i = t_i n', and 64 + 64 high products,
+# i.e. 136 + 2 * 128 = 392 low-multiply issue slots.
+IMAD_SLOTS_PER_CLK_PER_SM = 64
+IMAD_SLOTS_PER_FQ_MUL = 136 + 2 * 128
 FQ_MULS_PER_ADD = 6  # 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
-
-
-def fermat_inversion_muls():
-    """Field multiplications in the library's 4-bit fixed-window inversion of p - 2."""
-    p = 0x30644E72E131A029B85045B68181585D97816A916871CA8D3C208C16D87CFD47
-    nib = [int(ch, 16) for ch in "%064x" % (p - 2)]
-    first = next(i for i, v in enumerate(nib) if v)
-    sq = 4 * (len(nib) - 1 - first)
-    mul = sum(1 for v in nib[first + 1:] if v)
-    return 14 + sq + mul
 
 
 def parse():
@@ -281,11 +273,9 @@ def run_gpu(args, cfg):
     except OSError:
         pass
     sm_max_mhz = peaks.get("sm_max_mhz", 2070.0)
-    peak_timad = sms * IMAD_PER_CLK_PER_SM * sm_max_mhz * 1e6 / 1e12
-    strict_imad = adds_l0 * FQ_MULS_PER_ADD * IMAD_PER_FQ_MUL
+    peak_timad = sms * IMAD_SLOTS_PER_CLK_PER_SM * sm_max_mhz * 1e6 / 1e12
+    strict_imad = adds_l0 * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
     achieved = strict_imad / (l0_ms / 1e3) / 1e12
-    inv_muls = fermat_inversion_muls()
-    issued_imad = (adds_l0 * FQ_MULS_PER_ADD + adds_l0 / args.batch_s * inv_muls) * IMAD_PER_FQ_MUL
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
@@ -318,15 +308,16 @@ def run_gpu(args, cfg):
             "ms_per_msm": ms_per_step,
             "ms_median": statistics.median(step_ms),
             "phase_ms": mean_phase,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_timad, "unit": "TIMAD/s",
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_timad, "unit": "TIMADslot/s",
                          "frac": achieved / peak_timad, "traffic": traffic,
                          "kernel": "k_accum_level0",
-                         "peak_basis": "%d SMs x %d IMAD/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
-                                       % (sms, IMAD_PER_CLK_PER_SM, sm_max_mhz),
-                         "algorithmic_imad_per_launch": strict_imad,
+                         "peak_basis": "%d SMs x %d IMAD slots/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
+                                       % (sms, IMAD_SLOTS_PER_CLK_PER_SM, sm_max_mhz),
+                         "count_basis": "6 Fq muls per addition x 392 IMAD slots per mul (inversion excluded)",
+                         "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
-                         "issued_frac_incl_inversion": issued_imad / (l0_ms / 1e3) / 1e12 / peak_timad,
-                         "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_PER_FQ_MUL
+                         "inversion": "safegcd (Bernstein-Yang divsteps), one per %d additions" % args.batch_s,
+                         "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,
             "e2e": {"value": world * n / (e2e_ms / 1e3), "unit": "points/s", "ms_per_step": e2e_ms,

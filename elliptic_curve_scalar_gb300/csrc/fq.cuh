@@ -9,12 +9,13 @@
 // multiply-add pipe is the natural unit, so the limbs are 32-bit words and each
 // partial product is one mad.lo / mad.hi with the carry flag threaded through.
 //
-// Multiplication is coarsely integrated operand scanning (CIOS): for each
-// limb a_i, t += a_i*b, m = t_0 * (-p^-1 mod 2^32), t = (t + m*p) / 2^32.
-// Because p < 2^254, t stays below 2p < 2^255 between rounds, so a round never
-// carries past limb 8 and limb 8 is zero again after the shift; the result is
-// brought below p by one conditional subtraction.  Every carry chain sits in a
-// single asm statement so that nothing can clobber the carry flag inside it.
+// Multiplication is Montgomery's REDC on the full product (separated operand
+// scanning, see mul below).  Every carry chain sits in a single asm statement
+// so that nothing can clobber the carry flag inside it.  On this part the
+// multiply-high form of the 32-bit multiply-add issues at half the rate of
+// the low form, so a multiplication (136 low + 128 high products) costs about
+// 392 low-multiply issue slots; that mix is the roofline the kernels are
+// measured against.
 #pragma once
 #include <stdint.h>
 
@@ -149,67 +150,98 @@ __device__ __forceinline__ fe neg(const fe& a) {
 
 __device__ __forceinline__ fe dbl(const fe& a) { return add(a, a); }
 
-// One CIOS round: t := (t + ai*b + m*p) / 2^32 with m chosen so the low limb
-// cancels.  t holds 8 limbs on entry (limb 8 is implicitly zero).
-__device__ __forceinline__ void cios_round(uint32_t& t0, uint32_t& t1, uint32_t& t2, uint32_t& t3,
-                                           uint32_t& t4, uint32_t& t5, uint32_t& t6, uint32_t& t7,
-                                           uint32_t ai, const fe& b) {
-    asm("{\n\t"
-        ".reg .u32 t8, m;\n\t"
-        // t += lo(ai*b_j) at limb j
-        "mad.lo.cc.u32  %0, %8, %9,  %0;\n\t"
-        "madc.lo.cc.u32 %1, %8, %10, %1;\n\t"
-        "madc.lo.cc.u32 %2, %8, %11, %2;\n\t"
-        "madc.lo.cc.u32 %3, %8, %12, %3;\n\t"
-        "madc.lo.cc.u32 %4, %8, %13, %4;\n\t"
-        "madc.lo.cc.u32 %5, %8, %14, %5;\n\t"
-        "madc.lo.cc.u32 %6, %8, %15, %6;\n\t"
-        "madc.lo.cc.u32 %7, %8, %16, %7;\n\t"
-        "addc.u32       t8, 0, 0;\n\t"
-        // t += hi(ai*b_j) at limb j+1
-        "mad.hi.cc.u32  %1, %8, %9,  %1;\n\t"
-        "madc.hi.cc.u32 %2, %8, %10, %2;\n\t"
-        "madc.hi.cc.u32 %3, %8, %11, %3;\n\t"
-        "madc.hi.cc.u32 %4, %8, %12, %4;\n\t"
-        "madc.hi.cc.u32 %5, %8, %13, %5;\n\t"
-        "madc.hi.cc.u32 %6, %8, %14, %6;\n\t"
-        "madc.hi.cc.u32 %7, %8, %15, %7;\n\t"
-        "madc.hi.u32    t8, %8, %16, t8;\n\t"
-        // m = t0 * (-p^-1) mod 2^32
-        "mul.lo.u32     m, %0, %17;\n\t"
-        // t += lo(m*p_j) at limb j (limb 0 becomes zero)
-        "mad.lo.cc.u32  %0, m, %18, %0;\n\t"
-        "madc.lo.cc.u32 %1, m, %19, %1;\n\t"
-        "madc.lo.cc.u32 %2, m, %20, %2;\n\t"
-        "madc.lo.cc.u32 %3, m, %21, %3;\n\t"
-        "madc.lo.cc.u32 %4, m, %22, %4;\n\t"
-        "madc.lo.cc.u32 %5, m, %23, %5;\n\t"
-        "madc.lo.cc.u32 %6, m, %24, %6;\n\t"
-        "madc.lo.cc.u32 %7, m, %25, %7;\n\t"
-        "addc.u32       t8, t8, 0;\n\t"
-        // t += hi(m*p_j) at limb j+1, written one limb down (the division by 2^32)
-        "mad.hi.cc.u32  %0, m, %18, %1;\n\t"
-        "madc.hi.cc.u32 %1, m, %19, %2;\n\t"
-        "madc.hi.cc.u32 %2, m, %20, %3;\n\t"
-        "madc.hi.cc.u32 %3, m, %21, %4;\n\t"
-        "madc.hi.cc.u32 %4, m, %22, %5;\n\t"
-        "madc.hi.cc.u32 %5, m, %23, %6;\n\t"
-        "madc.hi.cc.u32 %6, m, %24, %7;\n\t"
-        "madc.hi.u32    %7, m, %25, t8;\n\t"
-        "}"
-        : "+r"(t0), "+r"(t1), "+r"(t2), "+r"(t3), "+r"(t4), "+r"(t5), "+r"(t6), "+r"(t7)
-        : "r"(ai), "r"(b.v[0]), "r"(b.v[1]), "r"(b.v[2]), "r"(b.v[3]), "r"(b.v[4]), "r"(b.v[5]), "r"(b.v[6]), "r"(b.v[7]),
-          "n"(FQ_NP0), "n"(FQ_P0), "n"(FQ_P1), "n"(FQ_P2), "n"(FQ_P3), "n"(FQ_P4), "n"(FQ_P5), "n"(FQ_P6), "n"(FQ_P7));
+// Row of partial products a_i * (b_0, b_2, b_4, b_6) (or the odd limbs of b)
+// added into t[0..7] as lo, hi, lo, hi, ...: one unbroken carry chain, with the
+// carry out added into t[8].
+__device__ __forceinline__ void mac_row4(uint32_t* t, uint32_t ai, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+    asm("mad.lo.cc.u32  %0, %9, %10, %0;\n\t"
+        "madc.hi.cc.u32 %1, %9, %10, %1;\n\t"
+        "madc.lo.cc.u32 %2, %9, %11, %2;\n\t"
+        "madc.hi.cc.u32 %3, %9, %11, %3;\n\t"
+        "madc.lo.cc.u32 %4, %9, %12, %4;\n\t"
+        "madc.hi.cc.u32 %5, %9, %12, %5;\n\t"
+        "madc.lo.cc.u32 %6, %9, %13, %6;\n\t"
+        "madc.hi.cc.u32 %7, %9, %13, %7;\n\t"
+        "addc.u32       %8, %8, 0;"
+        : "+r"(t[0]), "+r"(t[1]), "+r"(t[2]), "+r"(t[3]), "+r"(t[4]), "+r"(t[5]), "+r"(t[6]), "+r"(t[7]), "+r"(t[8])
+        : "r"(ai), "r"(b0), "r"(b1), "r"(b2), "r"(b3));
 }
 
-// a * b * R^-1 mod p
+// a * b * R^-1 mod p by separated operand scanning.  The 512-bit product is
+// built in two independent accumulators -- E for the even limbs of b, O for
+// the odd ones, one limb higher -- so that the two carry chains of each row
+// can overlap; E + O is then reduced by eight Montgomery rounds
+// t += m p 2^(32 i), m = t_i (-p^-1) mod 2^32.  A round's carry out of limb
+// i+8 belongs to limb i+9 and is added in the next round's chain.  T stays
+// below p^2 + p R < 2^511, and T / R < 2p needs one conditional subtraction.
 __device__ __forceinline__ fe mul(const fe& a, const fe& b) {
-    uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0, t4 = 0, t5 = 0, t6 = 0, t7 = 0;
+    uint32_t E[17], O[17];
 #pragma unroll
-    for (int i = 0; i < 8; i++) cios_round(t0, t1, t2, t3, t4, t5, t6, t7, a.v[i], b);
+    for (int i = 0; i < 17; i++) {
+        E[i] = 0;
+        O[i] = 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        mac_row4(E + i, a.v[i], b.v[0], b.v[2], b.v[4], b.v[6]);
+        mac_row4(O + i + 1, a.v[i], b.v[1], b.v[3], b.v[5], b.v[7]);
+    }
+    uint32_t T[17];
+    asm("add.cc.u32  %0, %17, %34;\n\t"
+        "addc.cc.u32 %1, %18, %35;\n\t"
+        "addc.cc.u32 %2, %19, %36;\n\t"
+        "addc.cc.u32 %3, %20, %37;\n\t"
+        "addc.cc.u32 %4, %21, %38;\n\t"
+        "addc.cc.u32 %5, %22, %39;\n\t"
+        "addc.cc.u32 %6, %23, %40;\n\t"
+        "addc.cc.u32 %7, %24, %41;\n\t"
+        "addc.cc.u32 %8, %25, %42;\n\t"
+        "addc.cc.u32 %9, %26, %43;\n\t"
+        "addc.cc.u32 %10, %27, %44;\n\t"
+        "addc.cc.u32 %11, %28, %45;\n\t"
+        "addc.cc.u32 %12, %29, %46;\n\t"
+        "addc.cc.u32 %13, %30, %47;\n\t"
+        "addc.cc.u32 %14, %31, %48;\n\t"
+        "addc.cc.u32 %15, %32, %49;\n\t"
+        "addc.u32    %16, %33, %50;"
+        : "=r"(T[0]), "=r"(T[1]), "=r"(T[2]), "=r"(T[3]), "=r"(T[4]), "=r"(T[5]), "=r"(T[6]), "=r"(T[7]), "=r"(T[8]),
+          "=r"(T[9]), "=r"(T[10]), "=r"(T[11]), "=r"(T[12]), "=r"(T[13]), "=r"(T[14]), "=r"(T[15]), "=r"(T[16])
+        : "r"(E[0]), "r"(E[1]), "r"(E[2]), "r"(E[3]), "r"(E[4]), "r"(E[5]), "r"(E[6]), "r"(E[7]), "r"(E[8]),
+          "r"(E[9]), "r"(E[10]), "r"(E[11]), "r"(E[12]), "r"(E[13]), "r"(E[14]), "r"(E[15]), "r"(E[16]),
+          "r"(O[0]), "r"(O[1]), "r"(O[2]), "r"(O[3]), "r"(O[4]), "r"(O[5]), "r"(O[6]), "r"(O[7]), "r"(O[8]),
+          "r"(O[9]), "r"(O[10]), "r"(O[11]), "r"(O[12]), "r"(O[13]), "r"(O[14]), "r"(O[15]), "r"(O[16]));
+    uint32_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        uint32_t m = T[i] * FQ_NP0;
+        asm("{\n\t.reg .u32 c;\n\t"
+            "mad.lo.cc.u32  %0, %10, %11, %0;\n\t"
+            "madc.lo.cc.u32 %1, %10, %12, %1;\n\t"
+            "madc.lo.cc.u32 %2, %10, %13, %2;\n\t"
+            "madc.lo.cc.u32 %3, %10, %14, %3;\n\t"
+            "madc.lo.cc.u32 %4, %10, %15, %4;\n\t"
+            "madc.lo.cc.u32 %5, %10, %16, %5;\n\t"
+            "madc.lo.cc.u32 %6, %10, %17, %6;\n\t"
+            "madc.lo.cc.u32 %7, %10, %18, %7;\n\t"
+            "addc.cc.u32    %8, %8, %9;\n\t"
+            "addc.u32       c, 0, 0;\n\t"
+            "mad.hi.cc.u32  %1, %10, %11, %1;\n\t"
+            "madc.hi.cc.u32 %2, %10, %12, %2;\n\t"
+            "madc.hi.cc.u32 %3, %10, %13, %3;\n\t"
+            "madc.hi.cc.u32 %4, %10, %14, %4;\n\t"
+            "madc.hi.cc.u32 %5, %10, %15, %5;\n\t"
+            "madc.hi.cc.u32 %6, %10, %16, %6;\n\t"
+            "madc.hi.cc.u32 %7, %10, %17, %7;\n\t"
+            "madc.hi.cc.u32 %8, %10, %18, %8;\n\t"
+            "addc.u32       %9, c, 0;\n\t"
+            "}"
+            : "+r"(T[i]), "+r"(T[i + 1]), "+r"(T[i + 2]), "+r"(T[i + 3]), "+r"(T[i + 4]), "+r"(T[i + 5]),
+              "+r"(T[i + 6]), "+r"(T[i + 7]), "+r"(T[i + 8]), "+r"(carry)
+            : "r"(m), "n"(FQ_P0), "n"(FQ_P1), "n"(FQ_P2), "n"(FQ_P3), "n"(FQ_P4), "n"(FQ_P5), "n"(FQ_P6), "n"(FQ_P7));
+    }
     fe r;
-    r.v[0] = t0; r.v[1] = t1; r.v[2] = t2; r.v[3] = t3;
-    r.v[4] = t4; r.v[5] = t5; r.v[6] = t6; r.v[7] = t7;
+#pragma unroll
+    for (int j = 0; j < 8; j++) r.v[j] = T[8 + j];
     reduce_once(r);
     return r;
 }

@@ -9,6 +9,7 @@
 // infinity) handled explicitly because those formulas do not cover them.
 #pragma once
 #include "fq.cuh"
+#include "inv.cuh"
 
 namespace g1 {
 
@@ -114,7 +115,7 @@ __device__ __forceinline__ jac add(const jac& p, const jac& q) {
 // Jacobian -> affine with one field inversion (infinity -> (0, 0)).
 __device__ __forceinline__ aff to_aff(const jac& p) {
     if (is_inf(p)) return aff_inf();
-    fe zi = fq::inv_fermat(p.Z);
+    fe zi = inv::inv_safegcd(p.Z);
     fe zi2 = fq::sqr(zi);
     return aff{fq::mul(p.X, zi2), fq::mul(p.Y, fq::mul(zi2, zi))};
 }

@@ -117,32 +117,46 @@ __global__ void __launch_bounds__(256) k_accum_level(uint32_t* __restrict__ item
     LevelSrc<S> src;
     src.items = items;
     src.half = half;
-    int count = 0, adds = 0, invs = 0;
+    int adds = 0, invs = 0;
+    // iterator over the pairs whose first item lies in [q0, q1): bucket g, next
+    // pair j in [j, jhi).  Batches are filled here and run below at one
+    // program point per round, so the lanes of a warp execute each batch (and
+    // its inversion) together instead of one divergent group after another.
+    const unsigned live = __activemask();
     uint32_t g = lo;
     uint32_t og = offsets[g] >> 1;
-    while (g < nb && og < q1) {
+    uint64_t j = 0, jhi = 0;
+    bool more = true;
+    auto enter_bucket = [&]() {
         uint32_t on = offsets[g + 1] >> 1;
-        uint32_t h = on - og;                                 // level-1 items of bucket g
-        uint32_t nl = (h + (1u << sh) - 1) >> sh;             // items at this level
-        uint32_t np = nl >> 1;                                // pairs at this level
-        if (np) {
-            uint64_t jlo = q0 > og ? (q0 - og + step - 1) >> level : 0;
-            uint64_t jhi = min((uint64_t)np, (q1 - og + step - 1) >> level);
-            for (uint64_t j = jlo; j < jhi; j++) {
+        uint32_t h = on - og;                                  // level-1 items of bucket g
+        uint32_t np = ((h + (1u << sh) - 1) >> sh) >> 1;       // pairs at this level
+        j = q0 > og ? (q0 - og + step - 1) >> level : 0;
+        jhi = min((uint64_t)np, (q1 - og + step - 1) >> level);
+        return on;
+    };
+    uint32_t on = enter_bucket();
+    for (;;) {
+        int count = 0;
+        while (count < S && more) {
+            if (j < jhi) {
                 src.qi[count++] = og + (uint32_t)(j << level);
-                if (count == S) {
-                    adds += batch_pairs<S>(src, count);
-                    invs++;
-                    count = 0;
+                j++;
+            } else {
+                g++;
+                og = on;
+                if (g >= nb || og >= q1) {
+                    more = false;
+                } else {
+                    on = enter_bucket();
                 }
             }
         }
-        g++;
-        og = on;
-    }
-    if (count) {
-        adds += batch_pairs<S>(src, count);
-        invs++;
+        if (__ballot_sync(live, count > 0) == 0) break;
+        if (count > 0) {
+            adds += batch_pairs<S>(src, count);
+            invs++;
+        }
     }
     if (stats) {
         warp_stats(ctl, adds, invs);
@@ -175,6 +189,7 @@ void launch_accum_level0(int batch_s, int tpb, const uint32_t* points, const uin
         case 2: level0_t<2>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
         case 4: level0_t<4>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
         case 16: level0_t<16>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
+        case 32: level0_t<32>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
         default: level0_t<8>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
     }
 }
@@ -186,6 +201,7 @@ void launch_accum_level(int batch_s, int tpb, uint32_t* items, const uint32_t* o
         case 2: level_t<2>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
         case 4: level_t<4>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
         case 16: level_t<16>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
+        case 32: level_t<32>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
         default: level_t<8>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
     }
 }

@@ -5,6 +5,7 @@
 
 #include "fq.cuh"
 #include "g1.cuh"
+#include "inv.cuh"
 
 namespace msm {
 
@@ -146,38 +147,40 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
 // Returns the number of slots that were true additions (ADD or DBL).
 template <int S, class Src>
 __device__ __forceinline__ int batch_pairs(Src& src, int count) {
+    // The per-slot loops stay rolled: unrolled, S copies of the inlined
+    // multiplications overflow the instruction cache (the kernel then stalls
+    // on instruction fetch) and pin S x 8 registers of prefix products.  The
+    // prefix products live in thread-local memory, which stays in L1.
     fe pre[S];
     fe acc = fq::one();
     int adds = 0;
-#pragma unroll
-    for (int k = 0; k < S; k++) {
-        fe d = fq::one();
-        if (k < count) {
-            bool hq = src.has_q(k);
-            fe xp = src.xp(k);
-            fe xq = hq ? src.xq(k) : fq::zero();
-            fe yp = fq::zero();
-            int cs = pair_case(hq, xp, xq, [&](fe& a, fe& b) { src.ys(k, a, b); }, yp);
-            d = pair_denominator(cs, xp, xq, yp);
-            adds += (cs == PC_ADD || cs == PC_DBL);
-        }
+#pragma unroll 1
+    for (int k = 0; k < count; k++) {
+        bool hq = src.has_q(k);
+        fe xp = src.xp(k);
+        fe xq = hq ? src.xq(k) : fq::zero();
+        fe yp = fq::zero();
+        int cs = pair_case(hq, xp, xq, [&](fe& a, fe& b) { src.ys(k, a, b); }, yp);
+        fe d = pair_denominator(cs, xp, xq, yp);
+        adds += (cs == PC_ADD || cs == PC_DBL);
         acc = (k == 0) ? d : fq::mul(acc, d);
         pre[k] = acc;
     }
-    fe inv = fq::inv_fermat(acc);
-#pragma unroll
-    for (int k = S - 1; k >= 0; k--) {
-        if (k < count) {
-            aff p = src.p(k);
-            bool hq = src.has_q(k);
-            aff q = hq ? src.q(k) : g1::aff_inf();
-            fe yp_unused = p.y;
-            int cs = pair_case(hq, p.x, q.x, [&](fe& a, fe& b) { a = p.y; b = q.y; }, yp_unused);
-            fe d = pair_denominator(cs, p.x, q.x, p.y);
-            fe dinv = (k > 0) ? fq::mul(inv, pre[k - 1]) : inv;
-            if (k > 0) inv = fq::mul(inv, d);
-            src.store(k, pair_result(cs, p, q, dinv));
+    fe inv = inv::inv_safegcd(acc);
+#pragma unroll 1
+    for (int k = count - 1; k >= 0; k--) {
+        aff p = src.p(k);
+        bool hq = src.has_q(k);
+        aff q = hq ? src.q(k) : g1::aff_inf();
+        fe yp_unused = p.y;
+        int cs = pair_case(hq, p.x, q.x, [&](fe& a, fe& b) { a = p.y; b = q.y; }, yp_unused);
+        fe d = pair_denominator(cs, p.x, q.x, p.y);
+        fe dinv = inv;
+        if (k > 0) {
+            dinv = fq::mul(inv, pre[k - 1]);
+            inv = fq::mul(inv, d);
         }
+        src.store(k, pair_result(cs, p, q, dinv));
     }
     return adds;
 }

@@ -469,7 +469,7 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
     if (!c) return MSM_G1_ERR_INVALID_ARG;
     switch (key) {
         case MSM_G1_PARAM_BATCH_S:
-            if (value != 1 && value != 2 && value != 4 && value != 8 && value != 16)
+            if (value != 1 && value != 2 && value != 4 && value != 8 && value != 16 && value != 32)
                 return MSM_G1_ERR_INVALID_ARG;
             c->batch_s = value;
             return MSM_G1_OK;

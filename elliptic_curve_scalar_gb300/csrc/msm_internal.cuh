@@ -20,7 +20,7 @@ struct ctl_t {
 };
 
 
-// accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16}
+// accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32}
 void launch_accum_level0(int batch_s, int tpb, const uint32_t* points, const uint32_t* entries, uint32_t* items,
                          ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st);
 void launch_accum_level(int batch_s, int tpb, uint32_t* items, const uint32_t* offsets, uint32_t nb, ctl_t* ctl,

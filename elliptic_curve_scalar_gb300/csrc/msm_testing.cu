@@ -23,6 +23,7 @@ __global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t
         case MSM_G1_TEST_FQ_ADD: r = fq::add(x, fq::load(b + 8 * i)); break;
         case MSM_G1_TEST_FQ_SUB: r = fq::sub(x, fq::load(b + 8 * i)); break;
         case MSM_G1_TEST_FQ_NEG: r = fq::neg(x); break;
+        case MSM_G1_TEST_FQ_INV: r = inv::inv_safegcd(x); break;
         default: r = fq::inv_fermat(x); break;
     }
     fq::store(out + 8 * i, r);
@@ -87,7 +88,7 @@ bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV) return MSM_G1_ERR_INVALID_ARG;
+    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV_FERMAT) return MSM_G1_ERR_INVALID_ARG;
     bool needs_b = op == MSM_G1_TEST_FQ_MUL || op == MSM_G1_TEST_FQ_ADD || op == MSM_G1_TEST_FQ_SUB;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
@@ -116,7 +117,7 @@ extern "C" int msm_g1_test_batch_add(const uint32_t* a, const uint32_t* b, uint3
         threads = (n + S - 1) / S;                                                               \
         k_test_batch_add<S><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n);    \
         break;
-        CASE(1) CASE(2) CASE(4) CASE(8) CASE(16)
+        CASE(1) CASE(2) CASE(4) CASE(8) CASE(16) CASE(32)
 #undef CASE
         default: return MSM_G1_ERR_INVALID_ARG;
     }

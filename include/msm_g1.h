@@ -54,7 +54,7 @@ extern "C" {
 #define MSM_G1_MAX_WINDOW 20
 
 /* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
-#define MSM_G1_PARAM_BATCH_S 1 /* additions sharing one inversion per thread: 1, 2, 4, 8, 16 (default 8) */
+#define MSM_G1_PARAM_BATCH_S 1 /* additions sharing one inversion per thread: 1, 2, 4, 8, 16, 32 (default 8) */
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */

@@ -73,7 +73,7 @@ def mid_case():
     return pts, k, expect_oracle(pts, k)
 
 
-@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("tpb", [64, 128, 256])
 def test_knobs(mid_case, batch_s, tpb):
     """Every batch size S and block size gives the same result (the pages
@@ -240,7 +240,7 @@ def test_config2_n65536_c13(big_points):
     assert np.array_equal(got, oracle.closed_form(r, k))
 
 
-@pytest.mark.parametrize("batch_s", [4, 8, 16])
+@pytest.mark.parametrize("batch_s", [4, 8, 16, 32])
 def test_config3_n2p20_c16(big_points, batch_s):
     r_all, pts_all = big_points
     n = 1 << 20

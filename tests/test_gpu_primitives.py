@@ -23,7 +23,7 @@ def _field_inputs(n, seed):
     return vals
 
 
-@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv"])
+@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv", "inv_fermat"])
 def test_fq_ops(op):
     n = 4099  # several blocks and a ragged tail
     a = _field_inputs(n, 1)
@@ -45,7 +45,7 @@ def test_fq_ops(op):
             e = (x - y) % P
         elif op == "neg":
             e = (-x) % P
-        else:
+        else:  # both inversions: 0 -> 0
             e = pow(x, P - 2, P)
         assert g == e, (op, x, y)
 
@@ -75,7 +75,7 @@ def test_jacobian_ops():
         assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
 
 
-@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32])
 def test_batch_affine_add(batch_s):
     """Batched affine pair additions, including pairs that would poison a
     shared inversion: equal points (tangent), opposite points, infinity."""
