@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="n2p16", choices=sorted(CONFIGS))
     ap.add_argument("--c", type=int, default=0, help="override the window size")
-    ap.add_argument("--batch-s", type=int, default=8)
+    ap.add_argument("--batch-s", type=int, default=32)
     ap.add_argument("--tpb", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()

@@ -174,7 +174,7 @@ __device__ __forceinline__ void mac_row4(uint32_t* t, uint32_t ai, uint32_t b0, 
 // t += m p 2^(32 i), m = t_i (-p^-1) mod 2^32.  A round's carry out of limb
 // i+8 belongs to limb i+9 and is added in the next round's chain.  T stays
 // below p^2 + p R < 2^511, and T / R < 2p needs one conditional subtraction.
-__device__ __forceinline__ fe mul(const fe& a, const fe& b) {
+__device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
     uint32_t E[17], O[17];
 #pragma unroll
     for (int i = 0; i < 17; i++) {
@@ -245,6 +245,13 @@ __device__ __forceinline__ fe mul(const fe& a, const fe& b) {
     reduce_once(r);
     return r;
 }
+
+// Called, not inlined: every kernel of the MSM runs long sequences of field
+// multiplications, and inlining each ~330-instruction body at every call site
+// makes the hot loops overflow the per-sub-partition instruction cache (the
+// warps then stall waiting for instruction fetch).  One shared body stays
+// resident.
+static __device__ __noinline__ fe mul(const fe& a, const fe& b) { return mul_inline(a, b); }
 
 __device__ __forceinline__ fe sqr(const fe& a) { return mul(a, a); }
 

@@ -52,7 +52,7 @@ struct s9 {
 __device__ __forceinline__ int32_t divsteps30(int32_t delta, uint32_t f, uint32_t g, int32_t& u_out, int32_t& v_out,
                                               int32_t& q_out, int32_t& r_out) {
     int32_t u = 1, v = 0, q = 0, r = 1;
-#pragma unroll
+#pragma unroll 5
     for (int i = 0; i < 30; i++) {
         // c1: delta > 0; c2: g odd
         int32_t c1 = (-delta) >> 31;

@@ -1,11 +1,25 @@
 // msm_accum.cu -- bucket accumulation by batched affine pair additions.
 //
-// Level 0 adds the two points of each even-aligned entry pair of the sorted
-// bucket list; level l >= 1 halves every bucket's remaining items in place.
-// Each thread runs its pairs in batches of S that share one field inversion
-// (Montgomery's trick, see batch_pairs in msm_core.cuh), the amortisation the
-// pages study as "walkerS" (PR #23736 "stream-walker -- amortize the field
-// inversion via large S + private pref_scratch", section "Goal & lever").
+// The buckets are reduced by a pair tree, the pages' level-wise accumulator
+// ("ba_fused_super", "the bin-packed pair-tree bucket-accumulate that runs for
+// every level of the MSM, with level 0 being the largest single dispatch",
+// PR #23520 "cache dx + idx in ba_fused_super pref_scratch", section "Summary"):
+//
+//  * level 0 adds the two entries of every even-aligned pair (2u, 2u+1) of the
+//    sorted bucket list (buckets are padded to even length, so a pair never
+//    straddles two buckets) and writes the sum to item u;
+//  * level l >= 1 adds items (q, q + 2^(l-1)) into q, halving every bucket's
+//    items in place until each bucket holds one point, its bucket sum.
+//
+// Which pairs exist at each level depends only on the bucket sizes, so one
+// kernel lists them for all levels up front (the pages' chunk_plan plays the
+// same role).  Every thread then takes a contiguous chunk of a level's list
+// and adds its pairs in batches that share one field inversion (Montgomery's
+// trick, batch_pairs in msm_core.cuh) -- the amortisation the pages study as
+// "walkerS" (PR #23736 "stream-walker -- amortize the field inversion via large
+// S + private pref_scratch", section "Goal & lever").  The chunk is
+// min(S, ceil(pairs / threads)): wide levels fill batches of S, narrow levels
+// spread their few pairs one per thread for the shortest latency.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,8 +41,10 @@ __device__ __forceinline__ void warp_stats(ctl_t* ctl, int adds, int invs) {
     }
 }
 
-// level 0: pair u = entries (2u, 2u+1) of the sorted list; operands are input
-// points gathered by index, negated when the entry's flag says so.
+// ------------------------------------------------------------------ level 0
+
+// pair u = entries (2u, 2u+1); operands are input points gathered by index,
+// negated when the entry's flag says so; a padding second entry means "copy".
 template <int S>
 struct Level0Src {
     const uint32_t* points;
@@ -57,17 +73,18 @@ __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict
                                                       const uint32_t* __restrict__ entries,
                                                       uint32_t* __restrict__ items, ctl_t* ctl, int stats) {
     const uint32_t units = ctl->total >> 1;
-    size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    size_t u0 = t * S;
+    const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t chunk = min((uint64_t)S, ((uint64_t)units + nthreads - 1) / nthreads);
+    const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t u0 = t * chunk;
     if (u0 >= units) return;
-    int count = (int)min((size_t)S, (size_t)units - u0);
+    const int count = (int)min(chunk, (uint64_t)units - u0);
     Level0Src<S> src;
     src.points = points;
     src.items = items;
     src.u0 = (uint32_t)u0;
-#pragma unroll
-    for (int k = 0; k < S; k++) {
-        uint2 e = k < count ? reinterpret_cast<const uint2*>(entries)[u0 + k] : make_uint2(HOLE, HOLE);
+    for (int k = 0; k < count; k++) {
+        uint2 e = reinterpret_cast<const uint2*>(entries)[u0 + k];
         src.e0[k] = e.x;
         src.e1[k] = e.y;
     }
@@ -75,13 +92,55 @@ __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict
     if (stats) warp_stats(ctl, adds, 1);
 }
 
-// level l >= 1: items of bucket g sit at o_g + i*2^(l-1) (o_g = offset_g / 2);
-// pair j is (o_g + j*2^l, o_g + j*2^l + 2^(l-1)) and its sum replaces the first.
+// ------------------------------------------------------- pair lists per level
+
+// Bucket g's level-1 items occupy [o_g, o_g + h_g) with o_g = offset_g / 2;
+// at level l it holds n_l = ceil(h_g / 2^(l-1)) items at stride 2^(l-1), which
+// form floor(n_l / 2) pairs, pair j starting at o_g + j 2^l.  One thread per
+// bucket; the lanes of a warp reserve list space with one atomic per level.
+__global__ void k_build_pairs(const uint32_t* __restrict__ offsets, uint32_t nb, uint32_t* __restrict__ pairs,
+                              PairLayout lay, ctl_t* ctl) {
+    const uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    uint32_t og = 0, h = 0;
+    if (g < nb) {
+        og = offsets[g] >> 1;
+        h = (offsets[g + 1] >> 1) - og;
+    }
+    for (int level = 1; level < MAX_LEVELS; level++) {
+        const int sh = level - 1;
+        uint32_t nl = h ? ((h - 1) >> sh) + 1 : 0;
+        uint32_t np = nl >> 1;
+        if (!__any_sync(0xffffffffu, np != 0)) break;
+        uint32_t incl = np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&ctl->pair_count[level], total);
+        base = __shfl_sync(0xffffffffu, base, 31);
+        uint32_t off = base + incl - np;
+        uint32_t* list = pairs + lay.base[level];
+        const uint32_t cap = lay.cap[level];
+        for (uint32_t j = 0; j < np; j++) {
+            uint32_t idx = off + j;
+            if (idx < cap) list[idx] = og + (j << level);
+            else atomicOr(&ctl->error, 1u);  // capacity bound violated (never expected)
+        }
+    }
+}
+
+// ------------------------------------------------------------- levels >= 1
+
+// pair (q, q + 2^(l-1)) of the level's list; its sum replaces the first item
 template <int S>
-struct LevelSrc {
+struct ListSrc {
     uint32_t* items;
     uint32_t half;
-    uint32_t qi[S];  // index of each pair's first item
+    uint32_t qi[S];
     __device__ __forceinline__ const uint32_t* a(int k) const { return items + (size_t)qi[k] * 16; }
     __device__ __forceinline__ const uint32_t* b(int k) const { return items + (size_t)(qi[k] + half) * 16; }
     __device__ __forceinline__ bool has_q(int) const { return true; }
@@ -97,113 +156,89 @@ struct LevelSrc {
 };
 
 template <int S>
-__global__ void __launch_bounds__(256) k_accum_level(uint32_t* __restrict__ items, const uint32_t* __restrict__ offsets,
-                                                     uint32_t nb, ctl_t* ctl, int level, int stats) {
-    const uint32_t step = 1u << level;
-    if (ctl->max_count <= step) return;  // every bucket already holds at most one item
-    const uint32_t H = ctl->total >> 1;  // level-1 index space
-    const uint64_t K = (uint64_t)S * step;
-    uint64_t q0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) * K;
-    if (q0 >= H) return;
-    uint64_t q1 = min(q0 + K, (uint64_t)H);
-    const uint32_t half = step >> 1;
-    const int sh = level - 1;
-    // last bucket g with o_g <= q0
-    uint32_t lo = 0, hi = nb;  // invariant: o_lo <= q0 < o_hi (o_nb = H)
-    while (hi - lo > 1) {
-        uint32_t mid = (lo + hi) >> 1;
-        if ((offsets[mid] >> 1) <= q0) lo = mid; else hi = mid;
-    }
-    LevelSrc<S> src;
+__global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
+                                                    ctl_t* ctl, int level, int stats) {
+    const uint32_t cnt = ctl->pair_count[level];
+    const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
+    const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t i0 = t * chunk;
+    if (i0 >= cnt) return;
+    const int count = (int)min(chunk, (uint64_t)cnt - i0);
+    ListSrc<S> src;
     src.items = items;
-    src.half = half;
-    int adds = 0, invs = 0;
-    // iterator over the pairs whose first item lies in [q0, q1): bucket g, next
-    // pair j in [j, jhi).  Batches are filled here and run below at one
-    // program point per round, so the lanes of a warp execute each batch (and
-    // its inversion) together instead of one divergent group after another.
-    const unsigned live = __activemask();
-    uint32_t g = lo;
-    uint32_t og = offsets[g] >> 1;
-    uint64_t j = 0, jhi = 0;
-    bool more = true;
-    auto enter_bucket = [&]() {
-        uint32_t on = offsets[g + 1] >> 1;
-        uint32_t h = on - og;                                  // level-1 items of bucket g
-        uint32_t np = ((h + (1u << sh) - 1) >> sh) >> 1;       // pairs at this level
-        j = q0 > og ? (q0 - og + step - 1) >> level : 0;
-        jhi = min((uint64_t)np, (q1 - og + step - 1) >> level);
-        return on;
-    };
-    uint32_t on = enter_bucket();
-    for (;;) {
-        int count = 0;
-        while (count < S && more) {
-            if (j < jhi) {
-                src.qi[count++] = og + (uint32_t)(j << level);
-                j++;
-            } else {
-                g++;
-                og = on;
-                if (g >= nb || og >= q1) {
-                    more = false;
-                } else {
-                    on = enter_bucket();
-                }
-            }
-        }
-        if (__ballot_sync(live, count > 0) == 0) break;
-        if (count > 0) {
-            adds += batch_pairs<S>(src, count);
-            invs++;
-        }
-    }
+    src.half = 1u << (level - 1);
+    for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
+    int adds = batch_pairs<S>(src, count);
     if (stats) {
-        warp_stats(ctl, adds, invs);
-        if (invs && threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
+        warp_stats(ctl, adds, 1);
+        if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
     }
 }
 
+// ----------------------------------------------------------------- launchers
+
+static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
+    // enough threads for chunks of S, but at least one resident wave when the
+    // level may hold that much work
+    uint64_t threads = std::max((work + S - 1) / S, std::min(work, resident));
+    return (unsigned)std::max<uint64_t>(1, (threads + tpb - 1) / tpb);
+}
 
 template <int S>
-static void level0_t(int tpb, const uint32_t* points, const uint32_t* entries, uint32_t* items, ctl_t* ctl,
-                     uint64_t units_ub, int stats, cudaStream_t st) {
-    uint64_t threads = (units_ub + S - 1) / S;
-    uint64_t blocks = std::max<uint64_t>(1, (threads + tpb - 1) / tpb);
-    k_accum_level0<S><<<(unsigned)blocks, tpb, 0, st>>>(points, entries, items, ctl, stats);
+static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries, uint32_t* items,
+                     ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, entries, items, ctl, stats);
 }
 
 template <int S>
-static void level_t(int tpb, uint32_t* items, const uint32_t* offsets, uint32_t nb, ctl_t* ctl, uint64_t h_ub,
-                    int level, int stats, cudaStream_t st) {
-    uint64_t K = (uint64_t)S << level;
-    uint64_t threads = (h_ub + K - 1) / K;
-    uint64_t blocks = std::max<uint64_t>(1, (threads + tpb - 1) / tpb);
-    k_accum_level<S><<<(unsigned)blocks, tpb, 0, st>>>(items, offsets, nb, ctl, level, stats);
+static void list_t(int tpb, uint64_t resident, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
+                   int level, int stats, cudaStream_t st) {
+    k_accum_list<S><<<grid_for(cap, S, tpb, resident), tpb, 0, st>>>(items, list, ctl, level, stats);
 }
 
-void launch_accum_level0(int batch_s, int tpb, const uint32_t* points, const uint32_t* entries, uint32_t* items,
-                         ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
+                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
     switch (batch_s) {
-        case 1: level0_t<1>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
-        case 2: level0_t<2>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
-        case 4: level0_t<4>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
-        case 16: level0_t<16>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
-        case 32: level0_t<32>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
-        default: level0_t<8>(tpb, points, entries, items, ctl, units_ub, stats, st); break;
+        case 1: level0_t<1>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        case 2: level0_t<2>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        case 4: level0_t<4>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        case 8: level0_t<8>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        case 16: level0_t<16>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        default: level0_t<32>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
     }
 }
 
-void launch_accum_level(int batch_s, int tpb, uint32_t* items, const uint32_t* offsets, uint32_t nb, ctl_t* ctl,
-                        uint64_t h_ub, int level, int stats, cudaStream_t st) {
+void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
+                        cudaStream_t st) {
+    k_build_pairs<<<(nb + 255) / 256, 256, 0, st>>>(offsets, nb, pairs, lay, ctl);
+}
+
+void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items, const uint32_t* pairs,
+                        const PairLayout& lay, ctl_t* ctl, int level, int stats, cudaStream_t st) {
+    const uint32_t* list = pairs + lay.base[level];
+    uint64_t cap = lay.cap[level];
     switch (batch_s) {
-        case 1: level_t<1>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
-        case 2: level_t<2>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
-        case 4: level_t<4>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
-        case 16: level_t<16>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
-        case 32: level_t<32>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
-        default: level_t<8>(tpb, items, offsets, nb, ctl, h_ub, level, stats, st); break;
+        case 1: list_t<1>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        case 2: list_t<2>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        case 4: list_t<4>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        case 8: list_t<8>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        case 16: list_t<16>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        default: list_t<32>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
     }
+}
+
+}  // namespace msm
+
+namespace msm {
+
+uint64_t accum_resident_threads(int tpb) {
+    int dev = 0, sms = 0, b0 = 0, b1 = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_accum_level0<32>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_accum_list<32>, tpb, 0);
+    return (uint64_t)sms * (uint64_t)std::max(1, std::min(b0, b1)) * (uint64_t)tpb;
 }
 
 }  // namespace msm

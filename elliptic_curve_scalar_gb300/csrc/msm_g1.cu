@@ -306,9 +306,12 @@ struct msm_g1_ctx {
     uint64_t cap_entries;  // padded entries
     uint64_t cap_buckets;  // W * B
     uint64_t cap_chunks;   // W * G
+    uint64_t cap_pairs;    // pair-list entries over all tree levels
     size_t scratch_bytes;
     char* scratch;
     uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
+    uint32_t* pairs;
+    uint64_t resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     ctl_t* ctl;
     bool gen_ready;
     int batch_s, tpb, timing, stats;
@@ -329,11 +332,31 @@ static uint32_t reduce_chunk_len(uint32_t B) {
 }
 
 struct sizing {
-    uint64_t entries, buckets, chunks;
+    uint64_t entries, buckets, chunks, pairs;
 };
 
+// Pair-list layout of the tree levels for at most h_ub level-1 items in nb
+// buckets: level l lists at most h_ub / 2^l + min(nb, h_ub / 2^(l-1)) / 2 pairs
+// (each bucket contributes floor(ceil(h / 2^(l-1)) / 2) <= h / 2^l + 1/2, and
+// only buckets with h > 2^(l-1) contribute).
+static PairLayout pair_layout(uint64_t h_ub, uint64_t nb, uint64_t* total) {
+    PairLayout lay;
+    uint64_t base = 0;
+    lay.base[0] = 0;
+    lay.cap[0] = 0;
+    for (int l = 1; l < MAX_LEVELS; l++) {
+        uint64_t live = std::min(nb, (h_ub >> (l - 1)) + 1);
+        uint64_t cap = (h_ub >> l) + 1 + (live + 1) / 2;
+        lay.base[l] = (uint32_t)base;
+        lay.cap[l] = (uint32_t)cap;
+        base += cap;
+    }
+    if (total) *total = base;
+    return lay;
+}
+
 static sizing size_for(size_t max_n, int max_c) {
-    sizing s{0, 0, 0};
+    sizing s{0, 0, 0, 0};
     int cmin = std::min(max_c, 8);
     s.entries = (uint64_t)max_n * window_count(cmin);
     for (int c = 1; c <= max_c; c++) {
@@ -345,6 +368,7 @@ static sizing size_for(size_t max_n, int max_c) {
     }
     s.entries += s.buckets;  // one padding entry per bucket at most
     s.entries += 2;
+    pair_layout((s.entries + 1) / 2, s.buckets, &s.pairs);
     return s;
 }
 
@@ -368,7 +392,9 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_wsums = take((size_t)96 * 256);
     size_t o_table = take((size_t)64 * 256);
     size_t o_tj = take((size_t)96 * 256);
+    size_t o_pairs = take((size_t)4 * s.pairs);
     if (assign) {
+        c->pairs = (uint32_t*)(c->scratch + o_pairs);
         c->ctl = (ctl_t*)(c->scratch + o_ctl);
         c->counts = (uint32_t*)(c->scratch + o_counts);
         c->offsets = (uint32_t*)(c->scratch + o_offsets);
@@ -428,7 +454,7 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     *out = nullptr;
     if (max_n < 1 || max_n > (1ull << 30) || max_c < 1 || max_c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
     sizing s = size_for(max_n, max_c);
-    if (s.entries >= (1ull << 31)) return MSM_G1_ERR_INVALID_ARG;  // offsets are 32-bit
+    if (s.entries >= (1ull << 31) || s.pairs >= (1ull << 32)) return MSM_G1_ERR_INVALID_ARG;  // 32-bit offsets
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MSM_G1_ERR_NO_DEVICE;
     cudaDeviceProp prop;
@@ -442,6 +468,7 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     c->cap_entries = s.entries;
     c->cap_buckets = s.buckets;
     c->cap_chunks = s.chunks;
+    c->cap_pairs = s.pairs;
     c->scratch_bytes = layout(nullptr, s, false);
     if (cudaMalloc((void**)&c->scratch, c->scratch_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -449,9 +476,12 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
         return MSM_G1_ERR_ALLOC;
     }
     layout(c, s, true);
-    c->batch_s = 8;
+    c->batch_s = 32;
     c->tpb = 128;
     c->timing = 0;
+    c->resident[0] = accum_resident_threads(64);
+    c->resident[1] = accum_resident_threads(128);
+    c->resident[2] = accum_resident_threads(256);
     *out = c;
     return MSM_G1_OK;
 }
@@ -545,7 +575,9 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     k_scan_reduce<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->ctl);
     k_scan_tiles<<<1, 1024, 0, st>>>(c->tile_sums, ntiles, c->ctl);
     k_scan_apply<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->offsets, c->cursor, c->entries, c->ctl);
-    launches += 3;
+    const PairLayout lay = pair_layout((entries_ub + 1) / 2, nb, nullptr);
+    launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
+    launches += 4;
     mark(2);
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
@@ -553,13 +585,15 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
         launches++;
     }
     mark(3);
-    launch_accum_level0(c->batch_s, c->tpb, points, c->entries, c->items, c->ctl, (entries_ub + 1) / 2, stats, st);
+    const uint64_t resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2];
+    launch_accum_level0(c->batch_s, c->tpb, resident, points, c->entries, c->items, c->ctl, (entries_ub + 1) / 2,
+                        stats, st);
     launches++;
     mark(4);
     // levels while some bucket may still hold two items: 2^level < max bucket <= n
     int levels = 0;
-    for (int level = 1; ((uint64_t)1 << level) < (uint64_t)n; level++) {
-        launch_accum_level(c->batch_s, c->tpb, c->items, c->offsets, nb, c->ctl, (entries_ub + 1) / 2, level, stats, st);
+    for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < (uint64_t)n; level++) {
+        launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, level, stats, st);
         levels++;
         launches++;
     }
@@ -598,9 +632,9 @@ extern "C" int msm_g1_last_stats(msm_g1_ctx* c, uint64_t* out, int nout) {
     CK(cudaSetDevice(c->device));
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));
-    uint64_t v[7] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
-                     (uint64_t)c->last_launches};
-    int k = std::min(nout, 7);
+    uint64_t v[8] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
+                     (uint64_t)c->last_launches, h.error};
+    int k = std::min(nout, 8);
     for (int i = 0; i < k; i++) out[i] = v[i];
     return k;
 }

@@ -32,7 +32,7 @@ PARAM_TIMING = 3
 PARAM_STATS = 4
 
 PHASES = ("digits", "scan", "scatter", "accum_l0", "accum_tree", "bucket_reduce", "combine")
-STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches")
+STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches", "error")
 
 TEST_FQ = {"mul": 0, "sqr": 1, "add": 2, "sub": 3, "neg": 4, "inv": 5, "inv_fermat": 6}
 TEST_G1 = {"jac_dbl": 0, "jac_add": 1, "jac_mixed": 2, "to_affine": 3}

@@ -54,7 +54,7 @@ extern "C" {
 #define MSM_G1_MAX_WINDOW 20
 
 /* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
-#define MSM_G1_PARAM_BATCH_S 1 /* additions sharing one inversion per thread: 1, 2, 4, 8, 16, 32 (default 8) */
+#define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32 (default 32) */
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
@@ -105,7 +105,8 @@ int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
  * digits), out[1] = non-empty buckets, out[2] = largest bucket; with
  * MSM_G1_PARAM_STATS = 1 also out[3] = affine additions performed by the
  * accumulation, out[4] = field inversions it performed, out[5] = tree levels
- * that had work (zero otherwise); out[6] = kernels the last run launched.
+ * that had work (zero otherwise); out[6] = kernels the last run launched;
+ * out[7] = non-zero if a device-side capacity check failed (never expected).
  * Returns the number of counters written (at most nout). */
 int msm_g1_last_stats(msm_g1_ctx *ctx, uint64_t *out, int nout);
 

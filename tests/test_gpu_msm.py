@@ -28,13 +28,15 @@ def ctx(max_n, max_c):
     return _ctx[key]
 
 
-def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=8, tpb=128):
+def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=32, tpb=128):
     n = k.shape[0]
     cx = ctx(max_n or max(n, 1), max_c or max(c, 1))
     cx.set_param(gm.PARAM_BATCH_S, batch_s)
     cx.set_param(gm.PARAM_TPB, tpb)
     out = cx.run(gpu_points(points_affine), gpu_scalars(k), c)
-    return normalise(out)
+    res = normalise(out)
+    assert cx.stats()["error"] == 0
+    return res
 
 
 def expect_oracle(points_affine, k):
