@@ -31,6 +31,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "../../include/msm_g1.h"
 #include "msm_internal.cuh"
@@ -675,4 +676,77 @@ extern "C" int msm_g1_debug_read(msm_g1_ctx* c, int which, void* dst, size_t max
     size_t k = std::min(sz, max_bytes);
     if (k) CK(cudaMemcpy(dst, src, k, cudaMemcpyDeviceToHost));
     return MSM_G1_OK;
+}
+
+// ====================================================== allocation-free entry
+//
+// msm_g1_run_noalloc serves callers that must not allocate device memory
+// themselves -- code whose device heap is owned by another allocator (a
+// framework's caching allocator that accounts for every byte), services with a
+// fixed memory budget, or hot paths that cannot afford cudaMalloc's implicit
+// device-wide synchronisation.  It runs the same kernels as msm_g1_run, with
+// all scratch carved from one fixed array in device global memory that every
+// GPU loading this library holds until the process exits.
+//
+// Host code must not take the array's name as a device address: the device
+// address of each GPU's copy is fetched once per device with
+// cudaGetSymbolAddress, with that device current, on the first call.
+
+#define NOALLOC_MAX_N 4096
+#define NOALLOC_MAX_C 10
+#define NOALLOC_SCRATCH_BYTES (8u << 20)
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocDevices = 64;
+std::mutex g_noalloc_lock;
+void* g_noalloc_ptr[kNoallocDevices];
+uint64_t g_noalloc_resident[kNoallocDevices][3];
+}  // namespace
+
+extern "C" int msm_g1_run_noalloc(const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
+                                  uint32_t* out, cudaStream_t stream) {
+    if (n > NOALLOC_MAX_N) return MSM_G1_ERR_CAPACITY;
+    int cw = window_c == 0 ? std::min(msm_g1_auto_window(n), NOALLOC_MAX_C) : window_c;
+    if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    if (cw > NOALLOC_MAX_C) return MSM_G1_ERR_CAPACITY;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocDevices) return MSM_G1_ERR_NO_DEVICE;
+    const sizing s = size_for(NOALLOC_MAX_N, NOALLOC_MAX_C);
+    if (layout(nullptr, s, false) > NOALLOC_SCRATCH_BYTES) return MSM_G1_ERR_CAPACITY;
+    {
+        std::lock_guard<std::mutex> guard(g_noalloc_lock);
+        if (!g_noalloc_ptr[dev]) {
+            cudaDeviceProp prop;
+            if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MSM_G1_ERR_NO_DEVICE;
+            if (prop.major != 10 || prop.minor != 3) return MSM_G1_ERR_NO_DEVICE;
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+                cudaGetLastError();
+                return MSM_G1_ERR_CUDA;
+            }
+            g_noalloc_resident[dev][0] = accum_resident_threads(64);
+            g_noalloc_resident[dev][1] = accum_resident_threads(128);
+            g_noalloc_resident[dev][2] = accum_resident_threads(256);
+            g_noalloc_ptr[dev] = ptr;
+        }
+    }
+    // a context on the host stack whose buffers all point into the fixed array
+    msm_g1_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.device = dev;
+    c.max_n = NOALLOC_MAX_N;
+    c.max_c = NOALLOC_MAX_C;
+    c.cap_entries = s.entries;
+    c.cap_buckets = s.buckets;
+    c.cap_chunks = s.chunks;
+    c.cap_pairs = s.pairs;
+    c.scratch = (char*)g_noalloc_ptr[dev];
+    c.scratch_bytes = NOALLOC_SCRATCH_BYTES;
+    layout(&c, s, true);
+    c.batch_s = 32;
+    c.tpb = 128;
+    for (int i = 0; i < 3; i++) c.resident[i] = g_noalloc_resident[dev][i];
+    return msm_g1_run(&c, points, scalars, n, cw, out, stream);
 }

@@ -44,6 +44,7 @@ _i = ctypes.c_int
 _SIGS = {
     "msm_g1_create": (_i, [ctypes.POINTER(_vp), _sz, _i]),
     "msm_g1_run": (_i, [_vp, _vp, _vp, _sz, _i, _vp, _vp]),
+    "msm_g1_run_noalloc": (_i, [_vp, _vp, _sz, _i, _vp, _vp]),
     "msm_g1_mul_generator": (_i, [_vp, _vp, _sz, _vp, _vp]),
     "msm_g1_destroy": (None, [_vp]),
     "msm_g1_set_param": (_i, [_vp, _i, _i]),
@@ -223,6 +224,21 @@ class MsmG1:
         _check(lib().msm_g1_debug_read(self._ctx, which, out.ctypes.data_as(ctypes.c_void_p), out.nbytes,
                                        ctypes.byref(nbytes)), "msm_g1_debug_read")
         return out, nbytes.value
+
+
+def run_noalloc(points, scalars, c=0, out=None, stream=None):
+    """msm_g1_run_noalloc: the MSM without a context, for n <= 4096 and c <= 10,
+    using the library's fixed device scratch array (see include/msm_g1.h)."""
+    n = scalars.shape[0]
+    if points.shape[0] != n:
+        raise ValueError("points and scalars differ in length")
+    pp = _dev_u32(points, (16,), "points")
+    sp = _dev_u32(scalars, (8,), "scalars")
+    if out is None:
+        out = torch.empty(24, dtype=torch.int32, device=points.device)
+    _check(lib().msm_g1_run_noalloc(pp, sp, n, c, ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)),
+           "msm_g1_run_noalloc")
+    return out
 
 
 # ----------------------------------------------------------------- test hooks

@@ -88,6 +88,24 @@ int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *s
 int msm_g1_mul_generator(msm_g1_ctx *ctx, const uint32_t *scalars, size_t n, uint32_t *out_points_affine,
                          cudaStream_t stream);
 
+/* The same MSM as msm_g1_run, for callers that cannot allocate device memory
+ * (their device heap is owned by another allocator, they run under a fixed
+ * memory budget, or they cannot afford cudaMalloc's implicit synchronisation).
+ * The source pages have no counterpart: this entry point exists for such
+ * callers only.  No context: all scratch comes from one fixed 8 MiB array in
+ * device global memory that the library holds on every GPU that loads it until
+ * the process exits.  Limits: n <= 4096 and window_c <= 10 (0 picks a window
+ * within that limit); larger n or c returns MSM_G1_ERR_CAPACITY without device
+ * work.  The first call on a device looks up the array's device address on
+ * that device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call reuses the same array: the calls clear what must start
+ * at zero themselves, but calls whose device work overlaps (different streams,
+ * or host threads, without ordering) race on the array and give wrong results.
+ * Inputs, output and stream as for msm_g1_run; a GPU of compute capability
+ * 10.3 is required (MSM_G1_ERR_NO_DEVICE otherwise). */
+int msm_g1_run_noalloc(const uint32_t *points_affine, const uint32_t *scalars, size_t n, int window_c,
+                       uint32_t *out_jacobian, cudaStream_t stream);
+
 /* Release the context's scratch (synchronises the device first).  NULL is a no-op. */
 void msm_g1_destroy(msm_g1_ctx *ctx);
 
