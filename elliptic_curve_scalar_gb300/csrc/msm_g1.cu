@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "../../include/msm_g1.h"
+#include "g1_coop.cuh"
 #include "msm_internal.cuh"
 
 using fq::fe;
@@ -248,14 +249,16 @@ __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* _
 
 // ---------------------------------------------------------- 7. combination
 
+// One warp: Horner's rule with warp-cooperative doublings and additions (the
+// chain of about 255 - c doublings is the latency floor of the whole MSM).
 __global__ void k_combine(const uint32_t* __restrict__ wsums, int W, int c, uint32_t* __restrict__ out) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
     jac q = g1::load_jac(wsums + (size_t)(W - 1) * 24);
     for (int w = W - 2; w >= 0; w--) {
-        for (int i = 0; i < c; i++) q = g1::dbl(q);
-        q = g1::add(q, g1::load_jac(wsums + (size_t)w * 24));
+        for (int i = 0; i < c; i++) q = g1c::dbl(q);
+        q = g1c::add(q, g1::load_jac(wsums + (size_t)w * 24));
     }
-    g1::store_jac(out, q);
+    if (threadIdx.x == 0) g1::store_jac(out, q);
 }
 
 __global__ void k_write_inf(uint32_t* out) {

@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include "../../include/msm_g1_testing.h"
+#include "g1_coop.cuh"
 #include "msm_core.cuh"
 
 using fq::fe;
@@ -42,6 +43,15 @@ __global__ void k_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t
             break;
         default: g1::store_aff(out + 16 * i, g1::to_aff(g1::load_jac(a + 24 * i))); break;
     }
+}
+
+// one warp per element, all lanes holding the same operands
+__global__ void k_test_g1_coop(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+    size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (i >= n) return;
+    jac r = op == MSM_G1_TEST_JAC_DBL_COOP ? g1c::dbl(g1::load_jac(a + 24 * i))
+                                           : g1c::add(g1::load_jac(a + 24 * i), g1::load_jac(b + 24 * i));
+    if ((threadIdx.x & 31) == 0) g1::store_jac(out + 24 * i, r);
 }
 
 template <int S>
@@ -98,11 +108,14 @@ extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint
 
 extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_TO_AFFINE) return MSM_G1_ERR_INVALID_ARG;
-    bool needs_b = op == MSM_G1_TEST_JAC_ADD || op == MSM_G1_TEST_JAC_MIXED;
+    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_ADD_COOP) return MSM_G1_ERR_INVALID_ARG;
+    bool needs_b = op == MSM_G1_TEST_JAC_ADD || op == MSM_G1_TEST_JAC_MIXED || op == MSM_G1_TEST_JAC_ADD_COOP;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
-    k_test_g1<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    if (op >= MSM_G1_TEST_JAC_DBL_COOP)
+        k_test_g1_coop<<<(unsigned)((n * 32 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    else
+        k_test_g1<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
     return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
 }
 

@@ -31,11 +31,14 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 
 /* Point operations.  JAC_* take and return Jacobian points (24 uint32),
  * MIXED adds a Jacobian a and an affine b, TO_AFFINE normalises a Jacobian a
- * into an affine out (16 uint32). */
+ * into an affine out (16 uint32).  *_COOP are the warp-cooperative doubling
+ * and addition of the window combination (one warp per element). */
 #define MSM_G1_TEST_JAC_DBL 0
 #define MSM_G1_TEST_JAC_ADD 1
 #define MSM_G1_TEST_JAC_MIXED 2
 #define MSM_G1_TEST_TO_AFFINE 3
+#define MSM_G1_TEST_JAC_DBL_COOP 4
+#define MSM_G1_TEST_JAC_ADD_COOP 5
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i

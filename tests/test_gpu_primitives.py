@@ -68,9 +68,18 @@ def test_jacobian_ops():
     add = gm.to_host(gm.test_g1("jac_add", da, db))
     mix = gm.to_host(gm.test_g1("jac_mixed", da, dab))
     aff = gm.to_host(gm.test_g1("to_affine", da))
+    dblc = gm.to_host(gm.test_g1("jac_dbl_coop", da))
+    addc = gm.to_host(gm.test_g1("jac_add_coop", da, db))
+    # the same sums with the operands of the special cases swapped and with P + P
+    addc2 = gm.to_host(gm.test_g1("jac_add_coop", db, da))
+    addc3 = gm.to_host(gm.test_g1("jac_add_coop", da, da))
     for i, (p, q) in enumerate(zip(a, b)):
         assert jac_words_to_point(dbl[i]) == pyref.add(p, p), ("dbl", i)
         assert jac_words_to_point(add[i]) == pyref.add(p, q), ("add", i)
+        assert jac_words_to_point(dblc[i]) == pyref.add(p, p), ("dbl_coop", i)
+        assert jac_words_to_point(addc[i]) == pyref.add(p, q), ("add_coop", i)
+        assert jac_words_to_point(addc2[i]) == pyref.add(q, p), ("add_coop swapped", i)
+        assert jac_words_to_point(addc3[i]) == pyref.add(p, p), ("add_coop P+P", i)
         assert jac_words_to_point(mix[i]) == pyref.add(p, q), ("mixed", i)
         assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
 
