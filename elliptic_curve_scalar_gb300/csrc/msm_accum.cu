@@ -71,14 +71,17 @@ struct Level0Src {
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict__ points,
                                                       const uint32_t* __restrict__ entries,
+                                                      const uint32_t* __restrict__ offsets, uint32_t g0, uint32_t g1,
                                                       uint32_t* __restrict__ items, ctl_t* ctl, int stats) {
-    const uint32_t units = ctl->total >> 1;
+    // units of buckets [g0, g1): pairs (2u, 2u+1) for u in [offset_g0 / 2, offset_g1 / 2)
+    const uint32_t ubeg = offsets[g0] >> 1;
+    const uint32_t units = (offsets[g1] >> 1) - ubeg;
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)units + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint64_t u0 = t * chunk;
-    if (u0 >= units) return;
-    const int count = (int)min(chunk, (uint64_t)units - u0);
+    const uint64_t u0 = ubeg + t * chunk;
+    if (t * chunk >= units) return;
+    const int count = (int)min(chunk, (uint64_t)units - t * chunk);
     Level0Src<S> src;
     src.points = points;
     src.items = items;
@@ -103,32 +106,61 @@ __global__ void k_build_pairs(const uint32_t* __restrict__ offsets, uint32_t nb,
     const uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     uint32_t og = 0, h = 0;
+    int grp = 0;
     if (g < nb) {
         og = offsets[g] >> 1;
         h = (offsets[g + 1] >> 1) - og;
+        const int w = (int)(g / lay.B);
+        while (grp + 1 < lay.groups && w < lay.w_lo[grp]) grp++;
     }
+    // lanes of one group share one atomic per level; a warp spanning two groups
+    // (only when B < 32) reserves per lane
+    const bool uniform = __match_any_sync(0xffffffffu, grp) == 0xffffffffu;
     for (int level = 1; level < MAX_LEVELS; level++) {
         const int sh = level - 1;
         uint32_t nl = h ? ((h - 1) >> sh) + 1 : 0;
         uint32_t np = nl >> 1;
         if (!__any_sync(0xffffffffu, np != 0)) break;
-        uint32_t incl = np;
+        uint32_t off;
+        if (uniform) {
+            uint32_t incl = np;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+            uint32_t base = 0;
+            if (lane == 31 && total) base = atomicAdd(&ctl->pair_count[grp][level], total);
+            base = __shfl_sync(0xffffffffu, base, 31);
+            off = base + incl - np;
+        } else {
+            off = np ? atomicAdd(&ctl->pair_count[grp][level], np) : 0;
         }
-        uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&ctl->pair_count[level], total);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        uint32_t off = base + incl - np;
-        uint32_t* list = pairs + lay.base[level];
-        const uint32_t cap = lay.cap[level];
-        for (uint32_t j = 0; j < np; j++) {
-            uint32_t idx = off + j;
-            if (idx < cap) list[idx] = og + (j << level);
-            else atomicOr(&ctl->error, 1u);  // capacity bound violated (never expected)
+        uint32_t* list = pairs + lay.base[grp][level];
+        const uint32_t cap = lay.cap[grp][level];
+        // long lists (a giant bucket) are written by the whole warp, short ones by their lane
+        constexpr uint32_t kLong = 64;
+        unsigned longs = __ballot_sync(0xffffffffu, np > kLong);
+        while (longs) {
+            const int src = __ffs(longs) - 1;
+            longs &= longs - 1;
+            const uint32_t nps = __shfl_sync(0xffffffffu, np, src);
+            const uint32_t offs = __shfl_sync(0xffffffffu, off, src);
+            const uint32_t ogs = __shfl_sync(0xffffffffu, og, src);
+            uint32_t* ls = pairs + lay.base[__shfl_sync(0xffffffffu, grp, src)][level];
+            const uint32_t caps = lay.cap[__shfl_sync(0xffffffffu, grp, src)][level];
+            for (uint32_t j = lane; j < nps; j += 32) {
+                if (offs + j < caps) ls[offs + j] = ogs + (j << level);
+                else atomicOr(&ctl->error, 1u);
+            }
+        }
+        if (np <= kLong) {
+            for (uint32_t j = 0; j < np; j++) {
+                uint32_t idx = off + j;
+                if (idx < cap) list[idx] = og + (j << level);
+                else atomicOr(&ctl->error, 1u);  // capacity bound violated (never expected)
+            }
         }
     }
 }
@@ -157,8 +189,8 @@ struct ListSrc {
 
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                    ctl_t* ctl, int level, int stats) {
-    const uint32_t cnt = ctl->pair_count[level];
+                                                    ctl_t* ctl, int grp, int level, int stats) {
+    const uint32_t cnt = ctl->pair_count[grp][level];
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -186,27 +218,32 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
 }
 
 template <int S>
-static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries, uint32_t* items,
-                     ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
-    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, entries, items, ctl, stats);
+static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
+                     const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items, ctl_t* ctl, uint64_t units_ub,
+                     int stats, cudaStream_t st) {
+    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, entries, offsets, g0, g1, items,
+                                                                           ctl, stats);
 }
 
 template <int S>
 static void list_t(int tpb, uint64_t resident, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
-                   int level, int stats, cudaStream_t st) {
-    k_accum_list<S><<<grid_for(cap, S, tpb, resident), tpb, 0, st>>>(items, list, ctl, level, stats);
+                   int grp, int level, int stats, cudaStream_t st) {
+    k_accum_list<S><<<grid_for(cap, S, tpb, resident), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
 }
 
 void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+                         const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items, ctl_t* ctl,
+                         uint64_t units_ub, int stats, cudaStream_t st) {
+#define L0(S) level0_t<S>(tpb, resident, points, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
     switch (batch_s) {
-        case 1: level0_t<1>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
-        case 2: level0_t<2>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
-        case 4: level0_t<4>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
-        case 8: level0_t<8>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
-        case 16: level0_t<16>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
-        default: level0_t<32>(tpb, resident, points, entries, items, ctl, units_ub, stats, st); break;
+        case 1: L0(1); break;
+        case 2: L0(2); break;
+        case 4: L0(4); break;
+        case 8: L0(8); break;
+        case 16: L0(16); break;
+        default: L0(32); break;
     }
+#undef L0
 }
 
 void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
@@ -215,17 +252,19 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
 }
 
 void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int level, int stats, cudaStream_t st) {
-    const uint32_t* list = pairs + lay.base[level];
-    uint64_t cap = lay.cap[level];
+                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st) {
+    const uint32_t* list = pairs + lay.base[grp][level];
+    uint64_t cap = lay.cap[grp][level];
+#define LV(S) list_t<S>(tpb, resident, items, list, ctl, cap, grp, level, stats, st)
     switch (batch_s) {
-        case 1: list_t<1>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
-        case 2: list_t<2>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
-        case 4: list_t<4>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
-        case 8: list_t<8>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
-        case 16: list_t<16>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
-        default: list_t<32>(tpb, resident, items, list, ctl, cap, level, stats, st); break;
+        case 1: LV(1); break;
+        case 2: LV(2); break;
+        case 4: LV(4); break;
+        case 8: LV(8); break;
+        case 16: LV(16); break;
+        default: LV(32); break;
     }
+#undef LV
 }
 
 }  // namespace msm

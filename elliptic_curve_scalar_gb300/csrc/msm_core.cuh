@@ -63,15 +63,29 @@ __device__ __forceinline__ uint32_t window_bits(const uint32_t k[8], int o, int 
     return (uint32_t)(two >> (o & 31)) & ((1u << c) - 1u);
 }
 
+// Window layout: W = ceil(255 / c) windows cover the 255 bits a signed-digit
+// recoding of k < r < 2^254 needs.  The top e = W c - 255 windows are one bit
+// narrower (c - 1 bits), so that no window is left with only a few bits -- a
+// short top window would hold few, very large buckets and deepen the
+// accumulation tree.  Window w covers bits [off_w, off_w + width_w).
+__host__ __device__ __forceinline__ int window_width(int w, int c, int W) {
+    return w >= W - (W * c - 255) ? c - 1 : c;
+}
+__host__ __device__ __forceinline__ int window_offset(int w, int c, int W) {
+    const int full = W - (W * c - 255);  // windows of c bits
+    return w <= full ? w * c : full * c + (w - full) * (c - 1);
+}
+
 // Signed digit of window w given the carry from window w-1: digits lie in
-// (-2^(c-1), 2^(c-1)]; a raw value above 2^(c-1) becomes raw - 2^c and carries
-// one into the next window.
-__device__ __forceinline__ int signed_digit(const uint32_t k[8], int w, int c, uint32_t& carry) {
-    uint32_t raw = window_bits(k, w * c, c) + carry;
-    uint32_t half = 1u << (c - 1);
+// (-2^(width-1), 2^(width-1)]; a raw value above 2^(width-1) becomes
+// raw - 2^width and carries one into the next window.
+__device__ __forceinline__ int signed_digit(const uint32_t k[8], int w, int c, int W, uint32_t& carry) {
+    const int cw = window_width(w, c, W);
+    uint32_t raw = window_bits(k, window_offset(w, c, W), cw) + carry;
+    uint32_t half = 1u << (cw - 1);
     if (raw > half) {
         carry = 1;
-        return (int)raw - (int)(1u << c);
+        return (int)raw - (int)(1u << cw);
     }
     carry = 0;
     return (int)raw;

@@ -96,7 +96,7 @@ __global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, in
     uint32_t carry = 0;
     int lane = threadIdx.x & 31;
     for (int w = 0; w < W; w++) {
-        int d = signed_digit(k, w, c, carry);
+        int d = signed_digit(k, w, c, W, carry);
         uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
         uint32_t peers = __match_any_sync(0xffffffffu, g);
         if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
@@ -193,7 +193,7 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
     int lane = threadIdx.x & 31;
     uint32_t lt_mask = (1u << lane) - 1u;
     for (int w = 0; w < W; w++) {
-        int d = signed_digit(k, w, c, carry);
+        int d = signed_digit(k, w, c, W, carry);
         uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
         uint32_t peers = __match_any_sync(0xffffffffu, g);
         int leader = __ffs(peers) - 1;
@@ -209,11 +209,11 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
 // One thread per chunk of L consecutive buckets of one window:
 // C_j = sum_{i<L} (jL + i + 1) S_{jL+i} via running sums from the top bucket.
 __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ counts,
-                                const uint32_t* __restrict__ offsets, int W, uint32_t B, uint32_t L,
+                                const uint32_t* __restrict__ offsets, int w_lo, int nwin, uint32_t B, uint32_t L,
                                 uint32_t G, uint32_t* __restrict__ chunks) {
     uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= (uint32_t)W * G) return;
-    uint32_t w = t / G, j = t % G;
+    if (t >= (uint32_t)nwin * G) return;
+    uint32_t w = (uint32_t)w_lo + t / G, j = t % G;
     uint32_t b0 = j * L;
     uint32_t b1 = min(b0 + L, B);
     jac run = g1::jac_inf(), sum = g1::jac_inf();
@@ -223,14 +223,14 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
         sum = g1::add(sum, run);
     }
     if (b0) sum = g1::add(sum, g1::mul_small(run, b0));
-    g1::store_jac(chunks + (size_t)t * 24, sum);
+    g1::store_jac(chunks + ((size_t)w * G + j) * 24, sum);
 }
 
 // One block per window: T_w = sum_j C_j (strided partial sums, then a tree).
-__global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* __restrict__ chunks, uint32_t G,
-                                                               uint32_t* __restrict__ wsums) {
+__global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* __restrict__ chunks, int w_lo,
+                                                               uint32_t G, uint32_t* __restrict__ wsums) {
     __shared__ uint32_t sm[REDUCE_TPB * 24];
-    uint32_t w = blockIdx.x;
+    uint32_t w = (uint32_t)w_lo + blockIdx.x;
     jac acc = g1::jac_inf();
     for (uint32_t j = threadIdx.x; j < G; j += blockDim.x)
         acc = g1::add(acc, g1::load_jac(chunks + ((size_t)w * G + j) * 24));
@@ -249,16 +249,20 @@ __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* _
 
 // ---------------------------------------------------------- 7. combination
 
-// One warp: Horner's rule with warp-cooperative doublings and additions (the
-// chain of about 255 - c doublings is the latency floor of the whole MSM).
-__global__ void k_combine(const uint32_t* __restrict__ wsums, int W, int c, uint32_t* __restrict__ out) {
+// One warp: Horner's rule over windows w_hi-1 .. w_lo with warp-cooperative
+// doublings and additions (the chain of about 255 - c doublings is the latency
+// floor of the whole MSM).  The running value is carried between window groups
+// in acc; the first group starts from its top window, the last writes out.
+__global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo, int c, int W,
+                               uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int first, int last) {
     if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    jac q = g1::load_jac(wsums + (size_t)(W - 1) * 24);
-    for (int w = W - 2; w >= 0; w--) {
-        for (int i = 0; i < c; i++) q = g1c::dbl(q);
+    jac q = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
+    for (int w = first ? w_hi - 2 : w_hi - 1; w >= w_lo; w--) {
+        // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
+        for (int i = window_width(w, c, W); i > 0; i--) q = g1c::dbl(q);
         q = g1c::add(q, g1::load_jac(wsums + (size_t)w * 24));
     }
-    if (threadIdx.x == 0) g1::store_jac(out, q);
+    if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
 }
 
 __global__ void k_write_inf(uint32_t* out) {
@@ -315,7 +319,12 @@ struct msm_g1_ctx {
     char* scratch;
     uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
     uint32_t* pairs;
+    uint32_t* qacc;        // running value of the window combination between groups
     uint64_t resident[3];  // resident accumulation threads for tpb = 64, 128, 256
+    int groups;            // window groups of the pipelined schedule (1 = serial)
+    bool streams_ok;       // the context's own streams and events exist
+    cudaStream_t acc_stream[2], chain_stream;
+    cudaEvent_t ev_fork, ev_group[MAX_GROUPS], ev_chain;
     ctl_t* ctl;
     bool gen_ready;
     int batch_s, tpb, timing, stats;
@@ -339,21 +348,37 @@ struct sizing {
     uint64_t entries, buckets, chunks, pairs;
 };
 
-// Pair-list layout of the tree levels for at most h_ub level-1 items in nb
-// buckets: level l lists at most h_ub / 2^l + min(nb, h_ub / 2^(l-1)) / 2 pairs
-// (each bucket contributes floor(ceil(h / 2^(l-1)) / 2) <= h / 2^l + 1/2, and
-// only buckets with h > 2^(l-1) contribute).
-static PairLayout pair_layout(uint64_t h_ub, uint64_t nb, uint64_t* total) {
+// Level pair-list capacities for at most h_ub level-1 items in nb buckets:
+// level l lists at most h_ub / 2^l + min(nb, h_ub / 2^(l-1)) / 2 pairs (a bucket
+// contributes floor(ceil(h / 2^(l-1)) / 2) <= h / 2^l + 1/2, and only buckets
+// with h > 2^(l-1) contribute).
+static uint64_t level_cap(uint64_t h_ub, uint64_t nb, int l) {
+    uint64_t live = std::min(nb, (h_ub >> (l - 1)) + 1);
+    return (h_ub >> l) + 1 + (live + 1) / 2;
+}
+
+// Window groups (top windows first) and their pair-list layout.
+static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_t* total) {
     PairLayout lay;
+    memset(&lay, 0, sizeof(lay));
+    groups = std::max(1, std::min(groups, std::min(W, MAX_GROUPS)));
+    lay.groups = groups;
+    lay.B = B;
+    const int per = (W + groups - 1) / groups;
     uint64_t base = 0;
-    lay.base[0] = 0;
-    lay.cap[0] = 0;
-    for (int l = 1; l < MAX_LEVELS; l++) {
-        uint64_t live = std::min(nb, (h_ub >> (l - 1)) + 1);
-        uint64_t cap = (h_ub >> l) + 1 + (live + 1) / 2;
-        lay.base[l] = (uint32_t)base;
-        lay.cap[l] = (uint32_t)cap;
-        base += cap;
+    for (int j = 0; j < groups; j++) {
+        lay.w_hi[j] = std::max(0, W - j * per);
+        lay.w_lo[j] = std::max(0, W - (j + 1) * per);
+        if (j == groups - 1) lay.w_lo[j] = 0;
+        const uint64_t nw = (uint64_t)(lay.w_hi[j] - lay.w_lo[j]);
+        const uint64_t nbj = nw * B;
+        const uint64_t h_ub = (n * nw + nbj + 1) / 2;
+        for (int l = 1; l < MAX_LEVELS; l++) {
+            uint64_t cap = nw ? level_cap(h_ub, nbj, l) : 0;
+            lay.base[j][l] = (uint32_t)base;
+            lay.cap[j][l] = (uint32_t)cap;
+            base += cap;
+        }
     }
     if (total) *total = base;
     return lay;
@@ -372,7 +397,16 @@ static sizing size_for(size_t max_n, int max_c) {
     }
     s.entries += s.buckets;  // one padding entry per bucket at most
     s.entries += 2;
-    pair_layout((s.entries + 1) / 2, s.buckets, &s.pairs);
+    // pair lists: the largest grouped layout over the windows this context allows
+    for (int c = 1; c <= max_c; c++) {
+        const int W = window_count(c);
+        const uint64_t n = std::min<uint64_t>(max_n, (s.entries - s.buckets) / W);
+        for (int groups = 1; groups <= MAX_GROUPS; groups++) {
+            uint64_t t = 0;
+            make_layout(n, W, 1u << (c - 1), groups, &t);
+            s.pairs = std::max(s.pairs, t);
+        }
+    }
     return s;
 }
 
@@ -397,8 +431,10 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_table = take((size_t)64 * 256);
     size_t o_tj = take((size_t)96 * 256);
     size_t o_pairs = take((size_t)4 * s.pairs);
+    size_t o_qacc = take((size_t)96);
     if (assign) {
         c->pairs = (uint32_t*)(c->scratch + o_pairs);
+        c->qacc = (uint32_t*)(c->scratch + o_qacc);
         c->ctl = (ctl_t*)(c->scratch + o_ctl);
         c->counts = (uint32_t*)(c->scratch + o_counts);
         c->offsets = (uint32_t*)(c->scratch + o_offsets);
@@ -486,6 +522,20 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     c->resident[0] = accum_resident_threads(64);
     c->resident[1] = accum_resident_threads(128);
     c->resident[2] = accum_resident_threads(256);
+    c->groups = MAX_GROUPS;
+    {
+        int lo = 0, hi = 0;
+        bool ok = cudaDeviceGetStreamPriorityRange(&lo, &hi) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[0], cudaStreamNonBlocking, lo) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[1], cudaStreamNonBlocking, lo) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&c->chain_stream, cudaStreamNonBlocking, hi) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&c->ev_chain, cudaEventDisableTiming) == cudaSuccess;
+        for (int j = 0; j < MAX_GROUPS; j++)
+            ok = ok && cudaEventCreateWithFlags(&c->ev_group[j], cudaEventDisableTiming) == cudaSuccess;
+        cudaGetLastError();
+        c->streams_ok = ok;  // without them every run takes the serial schedule
+    }
     *out = c;
     return MSM_G1_OK;
 }
@@ -495,6 +545,13 @@ void msm_g1_destroy(msm_g1_ctx* c) {
     cudaDeviceSynchronize();
     if (c->events_made)
         for (int i = 0; i <= kPhases; i++) cudaEventDestroy(c->ev[i]);
+    if (c->acc_stream[0]) cudaStreamDestroy(c->acc_stream[0]);
+    if (c->acc_stream[1]) cudaStreamDestroy(c->acc_stream[1]);
+    if (c->chain_stream) cudaStreamDestroy(c->chain_stream);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_chain) cudaEventDestroy(c->ev_chain);
+    for (int j = 0; j < MAX_GROUPS; j++)
+        if (c->ev_group[j]) cudaEventDestroy(c->ev_group[j]);
     cudaFree(c->scratch);
     free(c);
 }
@@ -519,6 +576,10 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
             c->stats = value;
             return MSM_G1_OK;
+        case MSM_G1_PARAM_GROUPS:
+            if (value < 1 || value > MAX_GROUPS) return MSM_G1_ERR_INVALID_ARG;
+            c->groups = value;
+            return MSM_G1_OK;
         default:
             return MSM_G1_ERR_INVALID_ARG;
     }
@@ -531,6 +592,7 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
         case MSM_G1_PARAM_TPB: *value = c->tpb; return MSM_G1_OK;
         case MSM_G1_PARAM_TIMING: *value = c->timing; return MSM_G1_OK;
         case MSM_G1_PARAM_STATS: *value = c->stats; return MSM_G1_OK;
+        case MSM_G1_PARAM_GROUPS: *value = c->groups; return MSM_G1_OK;
         default: return MSM_G1_ERR_INVALID_ARG;
     }
 }
@@ -579,7 +641,13 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     k_scan_reduce<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->ctl);
     k_scan_tiles<<<1, 1024, 0, st>>>(c->tile_sums, ntiles, c->ctl);
     k_scan_apply<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->offsets, c->cursor, c->entries, c->ctl);
-    const PairLayout lay = pair_layout((entries_ub + 1) / 2, nb, nullptr);
+    // Serial schedule (one stream, one window group) when phase timing is on --
+    // the phase events then delimit whole phases -- or when the context has no
+    // streams of its own; otherwise window groups are pipelined (below).
+    const bool pipelined = c->streams_ok && !c->timing && c->groups > 1 && W > 1;
+    uint64_t pairs_total = 0;
+    const PairLayout lay = make_layout(n, W, B, pipelined ? c->groups : 1, &pairs_total);
+    if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
     mark(2);
@@ -589,33 +657,70 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
         launches++;
     }
     mark(3);
-    const uint64_t resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2];
-    launch_accum_level0(c->batch_s, c->tpb, resident, points, c->entries, c->items, c->ctl, (entries_ub + 1) / 2,
-                        stats, st);
-    launches++;
-    mark(4);
-    // levels while some bucket may still hold two items: 2^level < max bucket <= n
-    int levels = 0;
-    for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < (uint64_t)n; level++) {
-        launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, level, stats, st);
-        levels++;
-        launches++;
-    }
-    c->last_levels = levels;
-    mark(5);
+    // two groups share the GPU in the pipelined schedule: size grids for half of it
+    const uint64_t resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2] / (pipelined ? 2 : 1);
     const uint32_t L = reduce_chunk_len(B);
     const uint32_t G = (B + L - 1) / L;
-    {
-        uint32_t threads = (uint32_t)W * G;
-        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, st>>>(c->items, c->counts, c->offsets, W, B, L, G, c->chunks);
-        k_reduce_windows<<<W, REDUCE_TPB, 0, st>>>(c->chunks, G, c->wsums);
+    // one window group: level 0, the tree levels, the bucket reduction
+    auto level0 = [&](int j, cudaStream_t s) {
+        const int nw = lay.w_hi[j] - lay.w_lo[j];
+        launch_accum_level0(c->batch_s, c->tpb, resident, points, c->entries, c->offsets, (uint32_t)lay.w_lo[j] * B,
+                            (uint32_t)lay.w_hi[j] * B, c->items, c->ctl, ((uint64_t)n * nw + (uint64_t)nw * B + 1) / 2,
+                            stats, s);
+        launches++;
+    };
+    auto tree = [&](int j, cudaStream_t s) {
+        // levels while some bucket may still hold two items: 2^level < max bucket <= n
+        for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < (uint64_t)n; level++) {
+            launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, j, level, stats, s);
+            launches++;
+        }
+    };
+    auto reduce = [&](int j, cudaStream_t s) {
+        const int nw = lay.w_hi[j] - lay.w_lo[j];
+        const uint32_t threads = (uint32_t)nw * G;
+        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, lay.w_lo[j], nw, B, L, G,
+                                                             c->chunks);
+        k_reduce_windows<<<nw, REDUCE_TPB, 0, s>>>(c->chunks, lay.w_lo[j], G, c->wsums);
         launches += 2;
+    };
+    auto combine = [&](int j, cudaStream_t s) {
+        k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], cw, W, c->qacc, out, j == 0,
+                                        j == lay.groups - 1);
+        launches++;
+    };
+    if (!pipelined) {
+        level0(0, st);
+        mark(4);
+        tree(0, st);
+        mark(5);
+        reduce(0, st);
+        mark(6);
+        combine(0, st);
+        mark(7);
+    } else {
+        // Window groups, top windows first, alternate between two accumulation
+        // streams; the combination chain runs on a high-priority stream and
+        // takes each group's window sums as soon as that group is done, so the
+        // long doubling chain overlaps the accumulation of the lower windows and
+        // the latency-bound tail of one group overlaps the next group's work.
+        CK(cudaEventRecord(c->ev_fork, st));
+        CK(cudaStreamWaitEvent(c->acc_stream[0], c->ev_fork, 0));
+        CK(cudaStreamWaitEvent(c->acc_stream[1], c->ev_fork, 0));
+        CK(cudaStreamWaitEvent(c->chain_stream, c->ev_fork, 0));
+        for (int j = 0; j < lay.groups; j++) {
+            cudaStream_t s = c->acc_stream[j & 1];
+            level0(j, s);
+            tree(j, s);
+            reduce(j, s);
+            CK(cudaEventRecord(c->ev_group[j], s));
+            CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
+            combine(j, c->chain_stream);
+        }
+        CK(cudaEventRecord(c->ev_chain, c->chain_stream));
+        CK(cudaStreamWaitEvent(st, c->ev_chain, 0));
     }
-    mark(6);
-    k_combine<<<1, 32, 0, st>>>(c->wsums, W, cw, out);
-    launches++;
     c->last_launches = launches;
-    mark(7);
     if (cudaGetLastError() != cudaSuccess) return MSM_G1_ERR_CUDA;
     c->have_timing = c->timing != 0;
     return MSM_G1_OK;

@@ -18,26 +18,34 @@ struct ctl_t {
     uint32_t levels;
     uint32_t error;       // non-zero if a device-side capacity check failed
     uint32_t pad[6];
-    uint32_t pair_count[32];  // pairs listed per tree level (index = level)
+    uint32_t pair_count[4][32];  // pairs listed per window group and tree level
 };
 
 constexpr int MAX_LEVELS = 32;
+constexpr int MAX_GROUPS = 4;
 
-// where each tree level's pair list starts in the pair buffer, and its capacity
+// Window groups: group j (j = 0 is the top) covers windows [w_lo[j], w_hi[j]);
+// each group's pair list for tree level l starts at base[j][l] in the pair
+// buffer and holds at most cap[j][l] entries.
 struct PairLayout {
-    uint32_t base[MAX_LEVELS];
-    uint32_t cap[MAX_LEVELS];
+    int groups;
+    uint32_t B;
+    int w_lo[MAX_GROUPS], w_hi[MAX_GROUPS];
+    uint32_t base[MAX_GROUPS][MAX_LEVELS];
+    uint32_t cap[MAX_GROUPS][MAX_LEVELS];
 };
 
 
 // accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32} is the
 // largest number of pairs a thread shares one inversion across
+// level 0 over the units of buckets [g0, g1); levels >= 1 over group grp's list
 void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st);
+                         const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items, ctl_t* ctl,
+                         uint64_t units_ub, int stats, cudaStream_t st);
 void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
                         cudaStream_t st);
 void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int level, int stats, cudaStream_t st);
+                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st);
 uint64_t accum_resident_threads(int tpb);
 
 }  // namespace msm

@@ -89,7 +89,7 @@ __global__ void k_test_digits(const uint32_t* scalars, size_t n, int c, int32_t*
     msm::reduce_mod_r(k);
     int W = msm::num_windows(c);
     uint32_t carry = 0;
-    for (int w = 0; w < W; w++) digits[i * W + w] = msm::signed_digit(k, w, c, carry);
+    for (int w = 0; w < W; w++) digits[i * W + w] = msm::signed_digit(k, w, c, W, carry);
 }
 
 bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }

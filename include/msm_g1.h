@@ -58,6 +58,7 @@ extern "C" {
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
+#define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4 (default 4) */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 
@@ -71,6 +72,9 @@ typedef struct msm_g1_ctx msm_g1_ctx;
 int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
 
 /* Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
+ * The context's own streams run the window groups concurrently; they are
+ * ordered after `stream` at the start and `stream` waits for them at the end,
+ * so to the caller the call behaves like work queued on `stream`.
  * points_affine: device, n x 16 uint32 (layout above), read only.
  * scalars: device, n x 8 uint32, read only.
  * window_c: 1..max_c, or 0 to let the library choose (msm_g1_auto_window).
@@ -116,7 +120,9 @@ int msm_g1_get_param(const msm_g1_ctx *ctx, int key, int *value);
 /* With MSM_G1_PARAM_TIMING = 1: wait for the last run and copy up to nphase
  * phase durations in milliseconds (decompose+histogram, scan, scatter,
  * accumulate level 0, accumulate levels >= 1, bucket reduction, window
- * combination) into ms.  Returns the number of phases written. */
+ * combination) into ms.  Returns the number of phases written.  Timing runs
+ * take the serial schedule (one stream, phases in order); otherwise the
+ * phases of different window groups overlap on the context's own streams. */
 int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
 
 /* Counters of the last run (waits for it): out[0] = bucket entries (non-zero

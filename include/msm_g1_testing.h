@@ -49,8 +49,10 @@ int msm_g1_test_batch_add(const uint32_t *a, const uint32_t *b, uint32_t *out, s
                           cudaStream_t stream);
 
 /* Signed window digits of n scalars (8 uint32 each) as the MSM forms them:
- * digits (n x ceil(255/c) int32, window-major per scalar) with each digit in
- * (-2^(c-1), 2^(c-1)] and sum_w digit_w 2^(c w) = k mod r. */
+ * digits (n x W int32, W = ceil(255/c), window-major per scalar).  Window w
+ * covers bits [off_w, off_w + c_w) with c_w = c for the lowest W - e windows
+ * and c - 1 for the top e = W c - 255 ones; each digit lies in
+ * (-2^(c_w - 1), 2^(c_w - 1)] and sum_w digit_w 2^off_w = k mod r. */
 int msm_g1_test_digits(const uint32_t *scalars, size_t n, int c, int32_t *digits, cudaStream_t stream);
 
 /* Copy an internal buffer of the last run to host memory (synchronises):

@@ -85,6 +85,25 @@ def test_knobs(mid_case, batch_s, tpb):
     assert np.array_equal(run_gpu(pts, k, 13, max_n=20000, max_c=13, batch_s=batch_s, tpb=tpb), expect)
 
 
+@pytest.mark.parametrize("groups", [1, 2, 3, 4])
+@pytest.mark.parametrize("timing", [0, 1])
+def test_window_groups_and_schedules(mid_case, groups, timing):
+    """The pipelined schedule (window groups on the context's streams) and the
+    serial one (phase timing on) give the same result for every group count."""
+    pts, k, expect = mid_case
+    cx = ctx(20000, 13)
+    cx.set_param(gm.PARAM_GROUPS, groups)
+    cx.set_param(gm.PARAM_TIMING, timing)
+    try:
+        got = normalise(cx.run(gpu_points(pts), gpu_scalars(k), 13))
+        if timing:
+            assert len(cx.phase_ms()) == 7
+    finally:
+        cx.set_param(gm.PARAM_GROUPS, 4)
+        cx.set_param(gm.PARAM_TIMING, 0)
+    assert np.array_equal(got, expect)
+
+
 def test_empty_input():
     cx = ctx(16, 8)
     pts = torch.zeros((0, 16), dtype=torch.int32, device="cuda")

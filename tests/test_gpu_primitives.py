@@ -111,6 +111,13 @@ def test_batch_affine_add(batch_s):
         assert aff_words_to_point(out[i]) == pyref.add(p, q), (batch_s, i)
 
 
+def window_layout(c):
+    """Widths of the W = ceil(255 / c) windows: the top W c - 255 are c - 1 bits."""
+    W = -(-255 // c)
+    narrow = W * c - 255
+    return [c - 1 if w >= W - narrow else c for w in range(W)]
+
+
 @pytest.mark.parametrize("c", [1, 2, 5, 8, 13, 16, 17, 18, 20])
 def test_signed_digits(c):
     rng = random.Random(c)
@@ -118,9 +125,10 @@ def test_signed_digits(c):
     ks += [rng.randrange(0, 1 << 256) for _ in range(300)]
     d = gm.test_digits(gm.to_device(ints_to_u32(ks)), c)
     digits = gm.to_host(d).view(np.int32)
+    widths = window_layout(c)
     W = gm.window_count(c)
-    assert digits.shape == (len(ks), W)
-    half = 1 << (c - 1)
+    assert digits.shape == (len(ks), W) and len(widths) == W and sum(widths) == 255
+    offsets = [sum(widths[:w]) for w in range(W)]
     for k, row in zip(ks, digits):
-        assert all(-half < int(v) <= half for v in row)
-        assert sum(int(v) << (c * w) for w, v in enumerate(row)) == k % R
+        assert all(-(1 << (cw - 1)) < int(v) <= (1 << (cw - 1)) for v, cw in zip(row, widths))
+        assert sum(int(v) << off for v, off in zip(row, offsets)) == k % R
