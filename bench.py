@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--c", type=int, default=0, help="override the window size")
     ap.add_argument("--batch-s", type=int, default=32)
     ap.add_argument("--tpb", type=int, default=128)
+    ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
+    ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -184,6 +186,8 @@ def run_gpu(args, cfg):
     ctx = gm.MsmG1(n, c)
     ctx.set_param(gm.PARAM_BATCH_S, args.batch_s)
     ctx.set_param(gm.PARAM_TPB, args.tpb)
+    ctx.set_param(gm.PARAM_FINISH, args.finish)
+    ctx.set_param(gm.PARAM_GROUPS, args.groups)
     scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
     # points P_i = [r_i]G built on the device by the library's fixed-base kernel
     pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
@@ -315,6 +319,7 @@ def run_gpu(args, cfg):
             "config": {"workload": "BN254 G1 MSM n=%d c=%d S=%d tpb=%d, %s points [r_i]G and scalars, seed %d"
                                    % (n, c, args.batch_s, args.tpb, cfg["kind"], cfg["seed"]),
                        "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"],
+                       "finish_t": args.finish or "auto", "groups": args.groups,
                        "l2": "flushed before every timed step (256 MiB write)", "replicas": world},
             "ms_per_msm": ms_per_step,
             "ms_median": statistics.median(step_ms),

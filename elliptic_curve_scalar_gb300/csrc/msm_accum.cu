@@ -119,7 +119,7 @@ __global__ void k_build_pairs(const uint32_t* __restrict__ offsets, uint32_t nb,
     for (int level = 1; level < MAX_LEVELS; level++) {
         const int sh = level - 1;
         uint32_t nl = h ? ((h - 1) >> sh) + 1 : 0;
-        uint32_t np = nl >> 1;
+        uint32_t np = nl > lay.finish_t ? nl >> 1 : 0;  // small buckets are finished in Jacobian
         if (!__any_sync(0xffffffffu, np != 0)) break;
         uint32_t off;
         if (uniform) {
@@ -206,6 +206,29 @@ __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items
         warp_stats(ctl, adds, 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
     }
+}
+
+// ------------------------------------------------------------ small buckets
+
+// One thread per bucket: buckets that left the tree with 2..T items get their
+// sum by Jacobian mixed additions (see finish_plan in msm_core.cuh).
+__global__ void k_finish(const uint32_t* __restrict__ items, const uint32_t* __restrict__ offsets, uint32_t g0,
+                         uint32_t g1, uint32_t finish_t, uint32_t* __restrict__ jsum) {
+    const uint32_t g = g0 + blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= g1) return;
+    const uint32_t og = offsets[g] >> 1;
+    const uint32_t h = (offsets[g + 1] >> 1) - og;
+    const FinishPlan fp = finish_plan(h, finish_t);
+    if (fp.items < 2) return;
+    g1::jac acc = g1::jac_inf();
+    for (uint32_t i = 0; i < fp.items; i++) acc = g1::add_mixed(acc, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
+    g1::store_jac(jsum + (size_t)g * 24, acc);
+}
+
+void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,
+                   uint32_t* jsum, cudaStream_t st) {
+    if (finish_t < 2 || g1 <= g0) return;
+    k_finish<<<(g1 - g0 + 127) / 128, 128, 0, st>>>(items, offsets, g0, g1, finish_t, jsum);
 }
 
 // ----------------------------------------------------------------- launchers

@@ -99,6 +99,27 @@ __device__ __forceinline__ void load_scalar(const uint32_t* s, uint32_t k[8]) {
 }
 
 // ---------------------------------------------------------------------------
+// Small-bucket finish.  A bucket with h level-1 items holds ceil(h / 2^(l-1))
+// items at tree level l.  It stays in the affine pair tree while that count
+// exceeds T; at the first level where it is at most T its items (stride
+// 2^(l-1)) are summed by one thread in Jacobian coordinates instead, which
+// needs no inversion and so avoids the per-level inversion latency of the
+// tree's narrow tail.  T = 1 keeps every bucket in the tree.
+struct FinishPlan {
+    uint32_t items;   // items left when the bucket leaves the tree
+    uint32_t stride;  // their spacing in the level-1 index space
+};
+
+__host__ __device__ __forceinline__ FinishPlan finish_plan(uint32_t h, uint32_t T) {
+    uint32_t stride = 1, items = h;
+    while (items > T) {
+        stride <<= 1;
+        items = (h + stride - 1) / stride;
+    }
+    return FinishPlan{items, stride};
+}
+
+// ---------------------------------------------------------------------------
 // Batched affine pair addition.
 //
 // A slot holds one pair (P, Q) and produces P + Q.  The denominator of the

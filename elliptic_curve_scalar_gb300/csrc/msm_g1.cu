@@ -209,8 +209,9 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
 // One thread per chunk of L consecutive buckets of one window:
 // C_j = sum_{i<L} (jL + i + 1) S_{jL+i} via running sums from the top bucket.
 __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ counts,
-                                const uint32_t* __restrict__ offsets, int w_lo, int nwin, uint32_t B, uint32_t L,
-                                uint32_t G, uint32_t* __restrict__ chunks) {
+                                const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ jsum,
+                                uint32_t finish_t, int w_lo, int nwin, uint32_t B, uint32_t L, uint32_t G,
+                                uint32_t* __restrict__ chunks) {
     uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= (uint32_t)nwin * G) return;
     uint32_t w = (uint32_t)w_lo + t / G, j = t % G;
@@ -219,7 +220,13 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
     jac run = g1::jac_inf(), sum = g1::jac_inf();
     for (uint32_t b = b1; b-- > b0;) {
         uint32_t g = w * B + b;
-        if (counts[g]) run = g1::add_mixed(run, g1::load_aff(items + (size_t)(offsets[g] >> 1) * 16));
+        if (counts[g]) {
+            const uint32_t og = offsets[g] >> 1;
+            if (finish_plan((offsets[g + 1] >> 1) - og, finish_t).items >= 2)
+                run = g1::add(run, g1::load_jac(jsum + (size_t)g * 24));  // finished in Jacobian
+            else
+                run = g1::add_mixed(run, g1::load_aff(items + (size_t)og * 16));
+        }
         sum = g1::add(sum, run);
     }
     if (b0) sum = g1::add(sum, g1::mul_small(run, b0));
@@ -320,10 +327,12 @@ struct msm_g1_ctx {
     uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
     uint32_t* pairs;
     uint32_t* qacc;        // running value of the window combination between groups
+    uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
+    int finish_t;          // 0: automatic
     uint64_t resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     int groups;            // window groups of the pipelined schedule (1 = serial)
     bool streams_ok;       // the context's own streams and events exist
-    cudaStream_t acc_stream[2], chain_stream;
+    cudaStream_t acc_stream[MAX_GROUPS], chain_stream;
     cudaEvent_t ev_fork, ev_group[MAX_GROUPS], ev_chain;
     ctl_t* ctl;
     bool gen_ready;
@@ -355,6 +364,15 @@ struct sizing {
 static uint64_t level_cap(uint64_t h_ub, uint64_t nb, int l) {
     uint64_t live = std::min(nb, (h_ub >> (l - 1)) + 1);
     return (h_ub >> l) + 1 + (live + 1) / 2;
+}
+
+// Automatic small-bucket threshold: small MSMs are latency-bound in the
+// narrow tail of the pair tree, large ones are throughput-bound throughout.
+static int auto_finish(uint64_t n, int W, uint64_t resident) {
+    const uint64_t pairs1 = n * (uint64_t)W / 4;  // about the level-1 pairs
+    if (pairs1 >= 8 * resident) return 1;
+    if (pairs1 >= 2 * resident) return 4;
+    return 8;
 }
 
 // Window groups (top windows first) and their pair-list layout.
@@ -432,7 +450,9 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_tj = take((size_t)96 * 256);
     size_t o_pairs = take((size_t)4 * s.pairs);
     size_t o_qacc = take((size_t)96);
+    size_t o_jsum = take((size_t)96 * s.buckets);
     if (assign) {
+        c->jsum = (uint32_t*)(c->scratch + o_jsum);
         c->pairs = (uint32_t*)(c->scratch + o_pairs);
         c->qacc = (uint32_t*)(c->scratch + o_qacc);
         c->ctl = (ctl_t*)(c->scratch + o_ctl);
@@ -522,12 +542,15 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     c->resident[0] = accum_resident_threads(64);
     c->resident[1] = accum_resident_threads(128);
     c->resident[2] = accum_resident_threads(256);
-    c->groups = MAX_GROUPS;
+    c->groups = 0;
     {
         int lo = 0, hi = 0;
         bool ok = cudaDeviceGetStreamPriorityRange(&lo, &hi) == cudaSuccess;
-        ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[0], cudaStreamNonBlocking, lo) == cudaSuccess;
-        ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[1], cudaStreamNonBlocking, lo) == cudaSuccess;
+        // accumulation streams at the lowest priority, the combination chain at
+        // the greatest, so its single-warp kernels start as soon as they may
+        // (graded priorities per group were measured slower at n = 2^22)
+        for (int j = 0; j < MAX_GROUPS; j++)
+            ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[j], cudaStreamNonBlocking, lo) == cudaSuccess;
         ok = ok && cudaStreamCreateWithPriority(&c->chain_stream, cudaStreamNonBlocking, hi) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->ev_chain, cudaEventDisableTiming) == cudaSuccess;
@@ -545,8 +568,8 @@ void msm_g1_destroy(msm_g1_ctx* c) {
     cudaDeviceSynchronize();
     if (c->events_made)
         for (int i = 0; i <= kPhases; i++) cudaEventDestroy(c->ev[i]);
-    if (c->acc_stream[0]) cudaStreamDestroy(c->acc_stream[0]);
-    if (c->acc_stream[1]) cudaStreamDestroy(c->acc_stream[1]);
+    for (int j = 0; j < MAX_GROUPS; j++)
+        if (c->acc_stream[j]) cudaStreamDestroy(c->acc_stream[j]);
     if (c->chain_stream) cudaStreamDestroy(c->chain_stream);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_chain) cudaEventDestroy(c->ev_chain);
@@ -577,8 +600,12 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             c->stats = value;
             return MSM_G1_OK;
         case MSM_G1_PARAM_GROUPS:
-            if (value < 1 || value > MAX_GROUPS) return MSM_G1_ERR_INVALID_ARG;
+            if (value < 0 || value > MAX_GROUPS) return MSM_G1_ERR_INVALID_ARG;
             c->groups = value;
+            return MSM_G1_OK;
+        case MSM_G1_PARAM_FINISH:
+            if (value < 0 || value > 64) return MSM_G1_ERR_INVALID_ARG;
+            c->finish_t = value;
             return MSM_G1_OK;
         default:
             return MSM_G1_ERR_INVALID_ARG;
@@ -593,6 +620,7 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
         case MSM_G1_PARAM_TIMING: *value = c->timing; return MSM_G1_OK;
         case MSM_G1_PARAM_STATS: *value = c->stats; return MSM_G1_OK;
         case MSM_G1_PARAM_GROUPS: *value = c->groups; return MSM_G1_OK;
+        case MSM_G1_PARAM_FINISH: *value = c->finish_t; return MSM_G1_OK;
         default: return MSM_G1_ERR_INVALID_ARG;
     }
 }
@@ -644,9 +672,11 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     // Serial schedule (one stream, one window group) when phase timing is on --
     // the phase events then delimit whole phases -- or when the context has no
     // streams of its own; otherwise window groups are pipelined (below).
-    const bool pipelined = c->streams_ok && !c->timing && c->groups > 1 && W > 1;
+    const int groups = c->groups ? c->groups : 2;  // two groups measured best (n = 2^16 .. 2^22)
+    const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1;
     uint64_t pairs_total = 0;
-    const PairLayout lay = make_layout(n, W, B, pipelined ? c->groups : 1, &pairs_total);
+    PairLayout lay = make_layout(n, W, B, pipelined ? groups : 1, &pairs_total);
+    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(n, W, c->resident[1]));
     if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
@@ -657,7 +687,7 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
         launches++;
     }
     mark(3);
-    // two groups share the GPU in the pipelined schedule: size grids for half of it
+    // the groups share the GPU in the pipelined schedule: size each grid for a share of it
     const uint64_t resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2] / (pipelined ? 2 : 1);
     const uint32_t L = reduce_chunk_len(B);
     const uint32_t G = (B + L - 1) / L;
@@ -679,8 +709,13 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     auto reduce = [&](int j, cudaStream_t s) {
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         const uint32_t threads = (uint32_t)nw * G;
-        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, lay.w_lo[j], nw, B, L, G,
-                                                             c->chunks);
+        if (lay.finish_t >= 2) {
+            launch_finish(c->items, c->offsets, (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, lay.finish_t,
+                          c->jsum, s);
+            launches++;
+        }
+        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum, lay.finish_t,
+                                                             lay.w_lo[j], nw, B, L, G, c->chunks);
         k_reduce_windows<<<nw, REDUCE_TPB, 0, s>>>(c->chunks, lay.w_lo[j], G, c->wsums);
         launches += 2;
     };
@@ -699,17 +734,16 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
         combine(0, st);
         mark(7);
     } else {
-        // Window groups, top windows first, alternate between two accumulation
-        // streams; the combination chain runs on a high-priority stream and
+        // Window groups, top windows first, each on its own accumulation
+        // stream; the combination chain runs on a high-priority stream and
         // takes each group's window sums as soon as that group is done, so the
         // long doubling chain overlaps the accumulation of the lower windows and
         // the latency-bound tail of one group overlaps the next group's work.
         CK(cudaEventRecord(c->ev_fork, st));
-        CK(cudaStreamWaitEvent(c->acc_stream[0], c->ev_fork, 0));
-        CK(cudaStreamWaitEvent(c->acc_stream[1], c->ev_fork, 0));
+        for (int j = 0; j < lay.groups; j++) CK(cudaStreamWaitEvent(c->acc_stream[j], c->ev_fork, 0));
         CK(cudaStreamWaitEvent(c->chain_stream, c->ev_fork, 0));
         for (int j = 0; j < lay.groups; j++) {
-            cudaStream_t s = c->acc_stream[j & 1];
+            cudaStream_t s = c->acc_stream[j];
             level0(j, s);
             tree(j, s);
             reduce(j, s);

@@ -30,6 +30,7 @@ constexpr int MAX_GROUPS = 4;
 struct PairLayout {
     int groups;
     uint32_t B;
+    uint32_t finish_t;  // buckets leave the affine tree once they hold <= finish_t items
     int w_lo[MAX_GROUPS], w_hi[MAX_GROUPS];
     uint32_t base[MAX_GROUPS][MAX_LEVELS];
     uint32_t cap[MAX_GROUPS][MAX_LEVELS];
@@ -47,5 +48,8 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
 void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items, const uint32_t* pairs,
                         const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st);
 uint64_t accum_resident_threads(int tpb);
+// Jacobian sums of the buckets of [g0, g1) that left the tree with >= 2 items
+void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,
+                   uint32_t* jsum, cudaStream_t st);
 
 }  // namespace msm

@@ -31,6 +31,7 @@ PARAM_TPB = 2
 PARAM_TIMING = 3
 PARAM_STATS = 4
 PARAM_GROUPS = 5
+PARAM_FINISH = 6
 
 PHASES = ("digits", "scan", "scatter", "accum_l0", "accum_tree", "bucket_reduce", "combine")
 STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches", "error")

@@ -58,7 +58,9 @@ extern "C" {
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
-#define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4 (default 4) */
+#define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = 2 (default) */
+#define MSM_G1_PARAM_FINISH 6  /* buckets with at most T items leave the affine tree and are summed in
+                                  Jacobian coordinates: T = 1..64, 1 = never, 0 = automatic (default) */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 

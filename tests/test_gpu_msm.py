@@ -99,8 +99,22 @@ def test_window_groups_and_schedules(mid_case, groups, timing):
         if timing:
             assert len(cx.phase_ms()) == 7
     finally:
-        cx.set_param(gm.PARAM_GROUPS, 4)
+        cx.set_param(gm.PARAM_GROUPS, 0)
         cx.set_param(gm.PARAM_TIMING, 0)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("finish_t", [1, 2, 3, 4, 8, 16, 64])
+def test_small_bucket_finish(mid_case, finish_t):
+    """Every small-bucket threshold T (buckets with <= T items summed in
+    Jacobian coordinates outside the affine tree) gives the same result."""
+    pts, k, expect = mid_case
+    cx = ctx(20000, 13)
+    cx.set_param(gm.PARAM_FINISH, finish_t)
+    try:
+        got = normalise(cx.run(gpu_points(pts), gpu_scalars(k), 13))
+    finally:
+        cx.set_param(gm.PARAM_FINISH, 0)
     assert np.array_equal(got, expect)
 
 
@@ -160,10 +174,17 @@ def test_progression_points(scal):
     assert np.array_equal(run_gpu(pts, k, 7), expect_oracle(pts, k))
 
 
-def test_adversarial_small():
+@pytest.mark.parametrize("finish_t", [1, 8])
+def test_adversarial_small(finish_t):
     r, k = synth.adversarial_workload(30000, 1005)
     pts = points_from_r(r)
-    assert np.array_equal(run_gpu(pts, k, 12, max_n=30000, max_c=16), expect_oracle(pts, k))
+    cx = ctx(30000, 16)
+    cx.set_param(gm.PARAM_FINISH, finish_t)
+    try:
+        got = run_gpu(pts, k, 12, max_n=30000, max_c=16)
+    finally:
+        cx.set_param(gm.PARAM_FINISH, 0)
+    assert np.array_equal(got, expect_oracle(pts, k))
 
 
 def test_deterministic_result():
