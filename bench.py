@@ -65,6 +65,7 @@ def parse():
     ap.add_argument("--tpb", type=int, default=128)
     ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
+    ap.add_argument("--glv", type=int, default=1, choices=[0, 1], help="split scalars by the GLV endomorphism")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -188,6 +189,7 @@ def run_gpu(args, cfg):
     ctx.set_param(gm.PARAM_TPB, args.tpb)
     ctx.set_param(gm.PARAM_FINISH, args.finish)
     ctx.set_param(gm.PARAM_GROUPS, args.groups)
+    ctx.set_param(gm.PARAM_GLV, args.glv)
     scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
     # points P_i = [r_i]G built on the device by the library's fixed-base kernel
     pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
@@ -204,7 +206,8 @@ def run_gpu(args, cfg):
     for _ in range(max(args.warmup, 3)):
         ctx.run(pts_d, scal_d, c, out=out_d)
     stats = ctx.stats()
-    counts, _ = ctx.debug_read(0, gm.window_count(c) * (1 << (c - 1)))
+    nwin = -(-(gm.GLV_BITS if args.glv else gm.PLAIN_BITS) // c)
+    counts, _ = ctx.debug_read(0, nwin * (1 << (c - 1)))
     ctx.set_param(gm.PARAM_STATS, 0)
     ctx.run(pts_d, scal_d, c, out=out_d)
     launches_per_msm = int(ctx.stats()["launches"])
@@ -316,9 +319,10 @@ def run_gpu(args, cfg):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) else None,
             "dtype": "u32", "data": "synthetic",
-            "config": {"workload": "BN254 G1 MSM n=%d c=%d S=%d tpb=%d, %s points [r_i]G and scalars, seed %d"
-                                   % (n, c, args.batch_s, args.tpb, cfg["kind"], cfg["seed"]),
-                       "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"],
+            "config": {"workload": "BN254 G1 MSM n=%d c=%d S=%d tpb=%d%s, %s points [r_i]G and scalars, seed %d"
+                                   % (n, c, args.batch_s, args.tpb, " GLV" if args.glv else "", cfg["kind"],
+                                      cfg["seed"]),
+                       "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"], "glv": args.glv,
                        "finish_t": args.finish or "auto", "groups": args.groups,
                        "l2": "flushed before every timed step (256 MiB write)", "replicas": world},
             "ms_per_msm": ms_per_step,

@@ -45,13 +45,19 @@ __device__ __forceinline__ void warp_stats(ctl_t* ctl, int adds, int invs) {
 
 // pair u = entries (2u, 2u+1); operands are input points gathered by index,
 // negated when the entry's flag says so; a padding second entry means "copy".
+// Indices from nsplit on address the GLV images phi(P_i) instead of P_i.
 template <int S>
 struct Level0Src {
     const uint32_t* points;
+    const uint32_t* phi;
+    uint32_t nsplit;
     uint32_t* items;
     uint32_t e0[S], e1[S];
     uint32_t u0;
-    __device__ __forceinline__ const uint32_t* pt(uint32_t e) const { return points + (size_t)(e & ~SIGN) * 16; }
+    __device__ __forceinline__ const uint32_t* pt(uint32_t e) const {
+        const uint32_t i = e & ~SIGN;
+        return i < nsplit ? points + (size_t)i * 16 : phi + (size_t)(i - nsplit) * 16;
+    }
     __device__ __forceinline__ bool has_q(int k) const { return e1[k] != HOLE; }
     __device__ __forceinline__ fe xp(int k) const { return fq::load(pt(e0[k])); }
     __device__ __forceinline__ fe xq(int k) const { return fq::load(pt(e1[k])); }
@@ -70,6 +76,7 @@ struct Level0Src {
 
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict__ points,
+                                                      const uint32_t* __restrict__ phi, uint32_t nsplit,
                                                       const uint32_t* __restrict__ entries,
                                                       const uint32_t* __restrict__ offsets, uint32_t g0, uint32_t g1,
                                                       uint32_t* __restrict__ items, ctl_t* ctl, int stats) {
@@ -84,6 +91,8 @@ __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict
     const int count = (int)min(chunk, (uint64_t)units - t * chunk);
     Level0Src<S> src;
     src.points = points;
+    src.phi = phi;
+    src.nsplit = nsplit;
     src.items = items;
     src.u0 = (uint32_t)u0;
     for (int k = 0; k < count; k++) {
@@ -241,11 +250,11 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
 }
 
 template <int S>
-static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
-                     const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items, ctl_t* ctl, uint64_t units_ub,
-                     int stats, cudaStream_t st) {
-    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, entries, offsets, g0, g1, items,
-                                                                           ctl, stats);
+static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
+                     const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
+                     ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, phi, nsplit, entries, offsets, g0,
+                                                                           g1, items, ctl, stats);
 }
 
 template <int S>
@@ -254,10 +263,11 @@ static void list_t(int tpb, uint64_t resident, uint32_t* items, const uint32_t* 
     k_accum_list<S><<<grid_for(cap, S, tpb, resident), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
 }
 
-void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* entries,
-                         const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items, ctl_t* ctl,
-                         uint64_t units_ub, int stats, cudaStream_t st) {
-#define L0(S) level0_t<S>(tpb, resident, points, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
+void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* phi,
+                         uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
+                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+#define L0(S) \
+    level0_t<S>(tpb, resident, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
     switch (batch_s) {
         case 1: L0(1); break;
         case 2: L0(2); break;

@@ -5,6 +5,7 @@
 
 #include "fq.cuh"
 #include "g1.cuh"
+#include "glv.cuh"
 #include "inv.cuh"
 
 namespace msm {
@@ -24,8 +25,6 @@ constexpr uint32_t SIGN = 0x80000000u;  // entry flag: negate the point
 #define FR_R5 0xb85045b6u
 #define FR_R6 0xe131a029u
 #define FR_R7 0x30644e72u
-
-__host__ __device__ constexpr int num_windows(int c) { return (255 + c - 1) / c; }
 
 // k := k mod r for any k < 2^256 (< 6r): subtract r while no borrow results.
 __device__ __forceinline__ void reduce_mod_r(uint32_t k[8]) {
@@ -49,39 +48,56 @@ __device__ __forceinline__ void reduce_mod_r(uint32_t k[8]) {
     }
 }
 
-__device__ __forceinline__ uint32_t limb_at(const uint32_t k[8], int i) {
+template <int NL>
+__device__ __forceinline__ uint32_t limb_at(const uint32_t (&k)[NL], int i) {
     uint32_t r = 0;
 #pragma unroll
-    for (int j = 0; j < 8; j++) r = (i == j) ? k[j] : r;
+    for (int j = 0; j < NL; j++) r = (i == j) ? k[j] : r;
     return r;
 }
 
-// c bits of k starting at bit o (bits past 255 read as zero)
-__device__ __forceinline__ uint32_t window_bits(const uint32_t k[8], int o, int c) {
+// c bits of k starting at bit o (bits past the last limb read as zero)
+template <int NL>
+__device__ __forceinline__ uint32_t window_bits(const uint32_t (&k)[NL], int o, int c) {
     int li = o >> 5;
     uint64_t two = (uint64_t)limb_at(k, li) | ((uint64_t)limb_at(k, li + 1) << 32);
     return (uint32_t)(two >> (o & 31)) & ((1u << c) - 1u);
 }
 
-// Window layout: W = ceil(255 / c) windows cover the 255 bits a signed-digit
-// recoding of k < r < 2^254 needs.  The top e = W c - 255 windows are one bit
-// narrower (c - 1 bits), so that no window is left with only a few bits -- a
-// short top window would hold few, very large buckets and deepen the
-// accumulation tree.  Window w covers bits [off_w, off_w + width_w).
-__host__ __device__ __forceinline__ int window_width(int w, int c, int W) {
-    return w >= W - (W * c - 255) ? c - 1 : c;
+// Window layout: W = ceil(nbits / c) windows cover the nbits bits that a
+// signed-digit recoding of the scalars needs (255 for k < r < 2^254; 128 for
+// the GLV halves |k_i| < 2^127).  The widths are balanced: the low rr windows
+// are q + 1 bits and the rest q bits, q = floor(nbits / W), rr = nbits - q W,
+// so that no window is left with only a few bits -- a short top window would
+// hold few, very large buckets and deepen the accumulation tree.  Every width
+// is at most c.  Window w covers bits [off_w, off_w + width_w).
+struct Windows {
+    int W, nbits, q, rr;
+};
+__host__ __device__ __forceinline__ Windows make_windows(int c, int nbits) {
+    Windows L;
+    L.W = (nbits + c - 1) / c;
+    L.nbits = nbits;
+    L.q = nbits / L.W;
+    L.rr = nbits - L.q * L.W;
+    return L;
 }
-__host__ __device__ __forceinline__ int window_offset(int w, int c, int W) {
-    const int full = W - (W * c - 255);  // windows of c bits
-    return w <= full ? w * c : full * c + (w - full) * (c - 1);
+__host__ __device__ __forceinline__ int window_width(const Windows& L, int w) { return w < L.rr ? L.q + 1 : L.q; }
+__host__ __device__ __forceinline__ int window_offset(const Windows& L, int w) {
+    return w <= L.rr ? w * (L.q + 1) : L.rr * (L.q + 1) + (w - L.rr) * L.q;
 }
+
+constexpr int PLAIN_BITS = 255;  // windows of the full scalar
+constexpr int GLV_BITS = 128;    // windows of one GLV half
 
 // Signed digit of window w given the carry from window w-1: digits lie in
 // (-2^(width-1), 2^(width-1)]; a raw value above 2^(width-1) becomes
-// raw - 2^width and carries one into the next window.
-__device__ __forceinline__ int signed_digit(const uint32_t k[8], int w, int c, int W, uint32_t& carry) {
-    const int cw = window_width(w, c, W);
-    uint32_t raw = window_bits(k, window_offset(w, c, W), cw) + carry;
+// raw - 2^width and carries one into the next window.  The top window never
+// carries out: the scalar's top bit (254, resp. 127) is zero.
+template <int NL>
+__device__ __forceinline__ int signed_digit(const uint32_t (&k)[NL], const Windows& L, int w, uint32_t& carry) {
+    const int cw = window_width(L, w);
+    uint32_t raw = window_bits(k, window_offset(L, w), cw) + carry;
     uint32_t half = 1u << (cw - 1);
     if (raw > half) {
         carry = 1;

@@ -81,26 +81,59 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sm, ui
 
 // ------------------------------------------------------ 1. digits + histogram
 
-// One thread per scalar; all lanes of a warp walk the windows together so that
-// lanes hitting the same bucket can share one atomic.
-__global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, int W,
-                              uint32_t* __restrict__ counts) {
-    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    bool live = i < n;
+// Visit every window digit of scalar i (k mod r; a dead lane sees k = 0 and
+// only zero digits): f(d, g, e) gets the digit, its bucket g = w B + |d| - 1
+// (HOLE for d = 0 or a dead lane) and its entry e, the point index with SIGN
+// set when the point enters negated.  With GLV, k P = k1 P + k2 phi(P): the
+// digits of |k1| go with point i, those of |k2| with point n + i (phi(P_i)),
+// each negated when its half is negative.  All lanes call f the same number
+// of times, so f may use warp collectives.
+template <bool GLV, class F>
+__device__ __forceinline__ void scalar_digits(const uint32_t* __restrict__ scalars, size_t n, size_t i, bool live,
+                                              int c, const Windows& L, F&& f) {
     uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (live) {
         load_scalar(scalars + 8 * i, k);
         reduce_mod_r(k);
     }
     const uint32_t B = 1u << (c - 1);
-    uint32_t carry = 0;
-    int lane = threadIdx.x & 31;
-    for (int w = 0; w < W; w++) {
-        int d = signed_digit(k, w, c, W, carry);
-        uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
-        uint32_t peers = __match_any_sync(0xffffffffu, g);
-        if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
+    auto visit = [&](auto& half, uint32_t e_base, uint32_t neg) {
+        uint32_t carry = 0;
+        for (int w = 0; w < L.W; w++) {
+            const int d = signed_digit(half, L, w, carry);
+            const uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
+            f(g, e_base | (((uint32_t)(d < 0) ^ neg) ? SIGN : 0u));
+        }
+    };
+    if constexpr (GLV) {
+        uint32_t k1[4], k2[4], neg1, neg2;
+        glv::split(k, k1, k2, neg1, neg2);
+        visit(k1, (uint32_t)i, neg1);
+        visit(k2, (uint32_t)(n + i), neg2);
+    } else {
+        visit(k, (uint32_t)i, 0u);
     }
+}
+
+// One thread per scalar; the lanes of a warp hitting the same bucket share one
+// atomic.  With GLV the kernel also writes phi(P_i) = (beta x_i, y_i).
+template <bool GLV>
+__global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L,
+                              uint32_t* __restrict__ counts, const uint32_t* __restrict__ points,
+                              uint32_t* __restrict__ phi) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool live = i < n;
+    if (GLV && live) {
+        const fe beta = {{GLV_BETA_MONT}};
+        aff p = g1::load_aff(points + 16 * i);
+        p.x = fq::mul(p.x, beta);  // the point at infinity (0, 0) stays (0, 0)
+        g1::store_aff(phi + 16 * i, p);
+    }
+    const int lane = threadIdx.x & 31;
+    scalar_digits<GLV>(scalars, n, i, live, c, L, [&](uint32_t g, uint32_t) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, g);
+        if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
+    });
 }
 
 // ---------------------------------------------------------------- 2. scan
@@ -179,29 +212,20 @@ __global__ void k_scan_apply(const uint32_t* __restrict__ counts, uint32_t nb, c
 
 // ------------------------------------------------------------- 3. scatter
 
-__global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c, int W,
+template <bool GLV>
+__global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L,
                           uint32_t* __restrict__ cursor, uint32_t* __restrict__ entries) {
-    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    bool live = i < n;
-    uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (live) {
-        load_scalar(scalars + 8 * i, k);
-        reduce_mod_r(k);
-    }
-    const uint32_t B = 1u << (c - 1);
-    uint32_t carry = 0;
-    int lane = threadIdx.x & 31;
-    uint32_t lt_mask = (1u << lane) - 1u;
-    for (int w = 0; w < W; w++) {
-        int d = signed_digit(k, w, c, W, carry);
-        uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
-        uint32_t peers = __match_any_sync(0xffffffffu, g);
-        int leader = __ffs(peers) - 1;
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    scalar_digits<GLV>(scalars, n, i, i < n, c, L, [&](uint32_t g, uint32_t e) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, g);
+        const int leader = __ffs(peers) - 1;
         uint32_t pos = 0;
         if (g != HOLE && lane == leader) pos = atomicAdd(&cursor[g], (uint32_t)__popc(peers));
         pos = __shfl_sync(0xffffffffu, pos, leader);
-        if (g != HOLE) entries[pos + __popc(peers & lt_mask)] = (uint32_t)i | (d < 0 ? SIGN : 0u);
-    }
+        if (g != HOLE) entries[pos + __popc(peers & lt_mask)] = e;
+    });
 }
 
 // ---------------------------------------------------------- 6. reduction
@@ -257,16 +281,16 @@ __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* _
 // ---------------------------------------------------------- 7. combination
 
 // One warp: Horner's rule over windows w_hi-1 .. w_lo with warp-cooperative
-// doublings and additions (the chain of about 255 - c doublings is the latency
+// doublings and additions (the chain of about nbits - c doublings is the latency
 // floor of the whole MSM).  The running value is carried between window groups
 // in acc; the first group starts from its top window, the last writes out.
-__global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo, int c, int W,
+__global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo, Windows L,
                                uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int first, int last) {
     if (blockIdx.x != 0 || threadIdx.x >= 32) return;
     jac q = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
     for (int w = first ? w_hi - 2 : w_hi - 1; w >= w_lo; w--) {
         // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
-        for (int i = window_width(w, c, W); i > 0; i--) q = g1c::dbl(q);
+        for (int i = window_width(L, w); i > 0; i--) q = g1c::dbl(q);
         q = g1c::add(q, g1::load_jac(wsums + (size_t)w * 24));
     }
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
@@ -328,6 +352,8 @@ struct msm_g1_ctx {
     uint32_t* pairs;
     uint32_t* qacc;        // running value of the window combination between groups
     uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
+    uint32_t* phi;         // phi(P_i) = (beta x_i, y_i) for the GLV split
+    int glv;               // 1: split scalars by the endomorphism (default)
     int finish_t;          // 0: automatic
     uint64_t resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     int groups;            // window groups of the pipelined schedule (1 = serial)
@@ -344,7 +370,8 @@ struct msm_g1_ctx {
     int last_levels;
 };
 
-static int window_count(int c) { return (255 + c - 1) / c; }
+static int window_count(int c) { return make_windows(c, PLAIN_BITS).W; }
+static int glv_window_count(int c) { return make_windows(c, GLV_BITS).W; }
 static uint32_t reduce_chunk_len(uint32_t B) {
     // L ~ sqrt(B / 512), a power of two, at least 4: balances the per-thread
     // running-sum chain against the per-window tree
@@ -354,7 +381,7 @@ static uint32_t reduce_chunk_len(uint32_t B) {
 }
 
 struct sizing {
-    uint64_t entries, buckets, chunks, pairs;
+    uint64_t points, entries, buckets, chunks, pairs;
 };
 
 // Level pair-list capacities for at most h_ub level-1 items in nb buckets:
@@ -403,9 +430,11 @@ static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_
 }
 
 static sizing size_for(size_t max_n, int max_c) {
-    sizing s{0, 0, 0, 0};
-    int cmin = std::min(max_c, 8);
-    s.entries = (uint64_t)max_n * window_count(cmin);
+    sizing s{max_n, 0, 0, 0, 0};
+    // entries for windows down to 8 bits (smaller windows fit smaller n); the
+    // GLV split doubles the terms and about halves the windows
+    const int cmin = std::min(max_c, 8);
+    s.entries = (uint64_t)max_n * std::max(window_count(cmin), 2 * glv_window_count(cmin));
     for (int c = 1; c <= max_c; c++) {
         uint64_t B = 1ull << (c - 1);
         uint64_t wb = (uint64_t)window_count(c) * B;
@@ -417,12 +446,14 @@ static sizing size_for(size_t max_n, int max_c) {
     s.entries += 2;
     // pair lists: the largest grouped layout over the windows this context allows
     for (int c = 1; c <= max_c; c++) {
-        const int W = window_count(c);
-        const uint64_t n = std::min<uint64_t>(max_n, (s.entries - s.buckets) / W);
-        for (int groups = 1; groups <= MAX_GROUPS; groups++) {
-            uint64_t t = 0;
-            make_layout(n, W, 1u << (c - 1), groups, &t);
-            s.pairs = std::max(s.pairs, t);
+        for (int glv = 0; glv <= 1; glv++) {
+            const int W = glv ? glv_window_count(c) : window_count(c);
+            const uint64_t terms = std::min<uint64_t>((uint64_t)max_n << glv, (s.entries - s.buckets) / W);
+            for (int groups = 1; groups <= MAX_GROUPS; groups++) {
+                uint64_t t = 0;
+                make_layout(terms, W, 1u << (c - 1), groups, &t);
+                s.pairs = std::max(s.pairs, t);
+            }
         }
     }
     return s;
@@ -451,7 +482,9 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_pairs = take((size_t)4 * s.pairs);
     size_t o_qacc = take((size_t)96);
     size_t o_jsum = take((size_t)96 * s.buckets);
+    size_t o_phi = take((size_t)64 * s.points);
     if (assign) {
+        c->phi = (uint32_t*)(c->scratch + o_phi);
         c->jsum = (uint32_t*)(c->scratch + o_jsum);
         c->pairs = (uint32_t*)(c->scratch + o_pairs);
         c->qacc = (uint32_t*)(c->scratch + o_qacc);
@@ -539,6 +572,7 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     c->batch_s = 32;
     c->tpb = 128;
     c->timing = 0;
+    c->glv = 1;
     c->resident[0] = accum_resident_threads(64);
     c->resident[1] = accum_resident_threads(128);
     c->resident[2] = accum_resident_threads(256);
@@ -607,6 +641,10 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             if (value < 0 || value > 64) return MSM_G1_ERR_INVALID_ARG;
             c->finish_t = value;
             return MSM_G1_OK;
+        case MSM_G1_PARAM_GLV:
+            if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
+            c->glv = value;
+            return MSM_G1_OK;
         default:
             return MSM_G1_ERR_INVALID_ARG;
     }
@@ -621,6 +659,7 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
         case MSM_G1_PARAM_STATS: *value = c->stats; return MSM_G1_OK;
         case MSM_G1_PARAM_GROUPS: *value = c->groups; return MSM_G1_OK;
         case MSM_G1_PARAM_FINISH: *value = c->finish_t; return MSM_G1_OK;
+        case MSM_G1_PARAM_GLV: *value = c->glv; return MSM_G1_OK;
         default: return MSM_G1_ERR_INVALID_ARG;
     }
 }
@@ -634,11 +673,15 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     int cw = window_c == 0 ? std::min(msm_g1_auto_window(n), c->max_c) : window_c;
     if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
     if (cw > c->max_c || n > c->max_n) return MSM_G1_ERR_CAPACITY;
-    const int W = window_count(cw);
+    // With GLV the MSM runs over 2n terms (P_i and phi(P_i)) with 128-bit windows.
+    const bool glv = c->glv != 0;
+    const Windows win = make_windows(cw, glv ? GLV_BITS : PLAIN_BITS);
+    const int W = win.W;
+    const uint64_t terms = glv ? 2 * (uint64_t)n : (uint64_t)n;
+    const uint32_t nsplit = glv ? (uint32_t)n : HOLE;  // entry indices >= nsplit address phi
     const uint32_t B = 1u << (cw - 1);
     const uint32_t nb = (uint32_t)W * B;
-    const uint64_t entries_ub = (uint64_t)n * W + nb;
-    if ((uint64_t)n * W + nb + 2 > c->cap_entries || nb > c->cap_buckets) return MSM_G1_ERR_CAPACITY;
+    if (terms * W + nb + 2 > c->cap_entries || nb > c->cap_buckets) return MSM_G1_ERR_CAPACITY;
     if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
     c->have_timing = false;
     if (c->timing && !c->events_made) {
@@ -661,7 +704,8 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
-        k_digits_hist<<<blocks, 256, 0, st>>>(scalars, n, cw, W, c->counts);
+        if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts, points, c->phi);
+        else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts, points, c->phi);
         launches++;
     }
     mark(1);
@@ -675,15 +719,16 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     const int groups = c->groups ? c->groups : 2;  // two groups measured best (n = 2^16 .. 2^22)
     const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1;
     uint64_t pairs_total = 0;
-    PairLayout lay = make_layout(n, W, B, pipelined ? groups : 1, &pairs_total);
-    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(n, W, c->resident[1]));
+    PairLayout lay = make_layout(terms, W, B, pipelined ? groups : 1, &pairs_total);
+    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, c->resident[1]));
     if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
     mark(2);
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
-        k_scatter<<<blocks, 256, 0, st>>>(scalars, n, cw, W, c->cursor, c->entries);
+        if (glv) k_scatter<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->cursor, c->entries);
+        else k_scatter<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->cursor, c->entries);
         launches++;
     }
     mark(3);
@@ -694,14 +739,14 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     // one window group: level 0, the tree levels, the bucket reduction
     auto level0 = [&](int j, cudaStream_t s) {
         const int nw = lay.w_hi[j] - lay.w_lo[j];
-        launch_accum_level0(c->batch_s, c->tpb, resident, points, c->entries, c->offsets, (uint32_t)lay.w_lo[j] * B,
-                            (uint32_t)lay.w_hi[j] * B, c->items, c->ctl, ((uint64_t)n * nw + (uint64_t)nw * B + 1) / 2,
-                            stats, s);
+        launch_accum_level0(c->batch_s, c->tpb, resident, points, c->phi, nsplit, c->entries, c->offsets,
+                            (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
+                            (terms * nw + (uint64_t)nw * B + 1) / 2, stats, s);
         launches++;
     };
     auto tree = [&](int j, cudaStream_t s) {
-        // levels while some bucket may still hold two items: 2^level < max bucket <= n
-        for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < (uint64_t)n; level++) {
+        // levels while some bucket may still hold two items: 2^level < max bucket <= terms
+        for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < terms; level++) {
             launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, j, level, stats, s);
             launches++;
         }
@@ -720,7 +765,7 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
         launches += 2;
     };
     auto combine = [&](int j, cudaStream_t s) {
-        k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], cw, W, c->qacc, out, j == 0,
+        k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
                                         j == lay.groups - 1);
         launches++;
     };
@@ -889,6 +934,7 @@ extern "C" int msm_g1_run_noalloc(const uint32_t* points, const uint32_t* scalar
     layout(&c, s, true);
     c.batch_s = 32;
     c.tpb = 128;
+    c.glv = 1;
     for (int i = 0; i < 3; i++) c.resident[i] = g_noalloc_resident[dev][i];
     return msm_g1_run(&c, points, scalars, n, cw, out, stream);
 }

@@ -81,15 +81,30 @@ __global__ void k_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t*
     msm::batch_pairs<S>(src, count);
 }
 
-__global__ void k_test_digits(const uint32_t* scalars, size_t n, int c, int32_t* digits) {
+__global__ void k_test_digits(const uint32_t* scalars, size_t n, int c, int nbits, int32_t* digits) {
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     uint32_t k[8];
     msm::load_scalar(scalars + 8 * i, k);
     msm::reduce_mod_r(k);
-    int W = msm::num_windows(c);
+    const msm::Windows L = msm::make_windows(c, nbits);
     uint32_t carry = 0;
-    for (int w = 0; w < W; w++) digits[i * W + w] = msm::signed_digit(k, w, c, W, carry);
+    for (int w = 0; w < L.W; w++) digits[i * L.W + w] = msm::signed_digit(k, L, w, carry);
+}
+
+__global__ void k_test_glv_split(const uint32_t* scalars, size_t n, uint32_t* out) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    uint32_t k[8], k1[4], k2[4], s1, s2;
+    msm::load_scalar(scalars + 8 * i, k);
+    msm::reduce_mod_r(k);
+    glv::split(k, k1, k2, s1, s2);
+    for (int j = 0; j < 4; j++) {
+        out[i * 10 + j] = k1[j];
+        out[i * 10 + 4 + j] = k2[j];
+    }
+    out[i * 10 + 8] = s1;
+    out[i * 10 + 9] = s2;
 }
 
 bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
@@ -137,10 +152,29 @@ extern "C" int msm_g1_test_batch_add(const uint32_t* a, const uint32_t* b, uint3
     return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
 }
 
-extern "C" int msm_g1_test_digits(const uint32_t* scalars, size_t n, int c, int32_t* digits, cudaStream_t st) {
+extern "C" int msm_g1_test_digits(const uint32_t* scalars, size_t n, int c, int nbits, int32_t* digits,
+                                  cudaStream_t st) {
     if (c < 1 || c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    if (nbits != msm::PLAIN_BITS && nbits != msm::GLV_BITS) return MSM_G1_ERR_INVALID_ARG;
     if (n == 0) return MSM_G1_OK;
     if (!scalars || !digits || !a16(scalars)) return MSM_G1_ERR_INVALID_ARG;
-    k_test_digits<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(scalars, n, c, digits);
+    k_test_digits<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(scalars, n, c, nbits, digits);
     return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_test_glv_split(const uint32_t* scalars, size_t n, uint32_t* out, cudaStream_t st) {
+    if (n == 0) return MSM_G1_OK;
+    if (!scalars || !out || !a16(scalars)) return MSM_G1_ERR_INVALID_ARG;
+    k_test_glv_split<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(scalars, n, out);
+    return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
+}
+
+extern "C" int msm_g1_glv_constants(uint32_t* beta_mont, uint32_t* lambda) {
+    if (!beta_mont || !lambda) return MSM_G1_ERR_INVALID_ARG;
+    const uint32_t b[8] = {GLV_BETA_MONT}, l[8] = {GLV_LAMBDA};
+    for (int j = 0; j < 8; j++) {
+        beta_mont[j] = b[j];
+        lambda[j] = l[j];
+    }
+    return MSM_G1_OK;
 }

@@ -32,6 +32,9 @@ PARAM_TIMING = 3
 PARAM_STATS = 4
 PARAM_GROUPS = 5
 PARAM_FINISH = 6
+PARAM_GLV = 7
+PLAIN_BITS = 255  # bits the signed windows of a scalar mod r cover
+GLV_BITS = 128    # bits the signed windows of one GLV half cover
 
 PHASES = ("digits", "scan", "scatter", "accum_l0", "accum_tree", "bucket_reduce", "combine")
 STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches", "error")
@@ -60,7 +63,9 @@ _SIGS = {
     "msm_g1_test_fq": (_i, [_i, _vp, _vp, _vp, _sz, _vp]),
     "msm_g1_test_g1": (_i, [_i, _vp, _vp, _vp, _sz, _vp]),
     "msm_g1_test_batch_add": (_i, [_vp, _vp, _vp, _sz, _i, _vp]),
-    "msm_g1_test_digits": (_i, [_vp, _sz, _i, _vp, _vp]),
+    "msm_g1_test_digits": (_i, [_vp, _sz, _i, _i, _vp, _vp]),
+    "msm_g1_test_glv_split": (_i, [_vp, _sz, _vp, _vp]),
+    "msm_g1_glv_constants": (_i, [_vp, _vp]),
     "msm_g1_debug_read": (_i, [_vp, _i, _vp, _sz, ctypes.POINTER(_sz)]),
 }
 
@@ -273,9 +278,27 @@ def test_batch_add(a, b, batch_s, stream=None):
     return out
 
 
-def test_digits(scalars, c, stream=None):
+def test_digits(scalars, c, nbits=PLAIN_BITS, stream=None):
     n = scalars.shape[0]
-    out = torch.empty((n, window_count(c)), dtype=torch.int32, device=scalars.device)
-    _check(lib().msm_g1_test_digits(ctypes.c_void_p(scalars.data_ptr()), n, c, ctypes.c_void_p(out.data_ptr()),
-                                    _stream_handle(stream)), "msm_g1_test_digits")
+    out = torch.empty((n, -(-nbits // c)), dtype=torch.int32, device=scalars.device)
+    _check(lib().msm_g1_test_digits(ctypes.c_void_p(scalars.data_ptr()), n, c, nbits,
+                                    ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)), "msm_g1_test_digits")
     return out
+
+
+def test_glv_split(scalars, stream=None):
+    """(n, 10) uint32 words per scalar: |k1| (4), |k2| (4), sign of k1, sign of k2."""
+    n = scalars.shape[0]
+    out = torch.empty((n, 10), dtype=torch.int32, device=scalars.device)
+    _check(lib().msm_g1_test_glv_split(ctypes.c_void_p(scalars.data_ptr()), n, ctypes.c_void_p(out.data_ptr()),
+                                       _stream_handle(stream)), "msm_g1_test_glv_split")
+    return out
+
+
+def glv_constants():
+    """(beta in Montgomery form, lambda) as Python ints, read from the library
+    (host only)."""
+    beta = (ctypes.c_uint32 * 8)()
+    lam = (ctypes.c_uint32 * 8)()
+    _check(lib().msm_g1_glv_constants(beta, lam), "msm_g1_glv_constants")
+    return (sum(int(v) << (32 * j) for j, v in enumerate(beta)), sum(int(v) << (32 * j) for j, v in enumerate(lam)))

@@ -61,19 +61,27 @@ extern "C" {
 #define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = 2 (default) */
 #define MSM_G1_PARAM_FINISH 6  /* buckets with at most T items leave the affine tree and are summed in
                                   Jacobian coordinates: T = 1..64, 1 = never, 0 = automatic (default) */
+#define MSM_G1_PARAM_GLV 7     /* 1: split every scalar by the curve endomorphism (default), 0: plain windows */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 
 /* Create a context on the current CUDA device and allocate its device
  * scratch (one allocation, owned by the context).  Scratch covers every run
- * with n <= max_n and c <= max_c whose entry count n * ceil(255/c) is at most
- * max_n * ceil(255/min(8, max_c)); msm_g1_scratch_bytes gives the size.
+ * with n <= max_n and c <= max_c whose entry count (n * ceil(255/c) plain,
+ * 2n * ceil(128/c) with the GLV split) is at most
+ * max_n * max(ceil(255/c8), 2 ceil(128/c8)), c8 = min(8, max_c); every c >= c8
+ * qualifies.  msm_g1_scratch_bytes gives the size.
  * max_c in [1, MSM_G1_MAX_WINDOW]; max_n in [1, 2^30].  Synchronous.
  * Returns MSM_G1_ERR_NO_DEVICE without a usable GPU, MSM_G1_ERR_ALLOC when the
  * allocation fails.  On error *ctx is set to NULL. */
 int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
 
 /* Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
+ * With MSM_G1_PARAM_GLV = 1 (the default) each term is split by the
+ * endomorphism phi(x, y) = (beta x, y) = [lambda](x, y) of BN254 G1 into
+ * k1 P + k2 phi(P) with |k1|, |k2| < 2^127 (Gallant-Lambert-Vanstone), so the
+ * bucket method runs over 2n terms with ceil(128/c) windows of c bits instead
+ * of n terms with ceil(255/c) windows; the result is the same point.
  * The context's own streams run the window groups concurrently; they are
  * ordered after `stream` at the start and `stream` waits for them at the end,
  * so to the caller the call behaves like work queued on `stream`.
@@ -137,7 +145,8 @@ int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
 int msm_g1_last_stats(msm_g1_ctx *ctx, uint64_t *out, int nout);
 
 /* Host-only helpers (no device work). */
-int msm_g1_window_count(int c);                      /* ceil(255 / c): signed windows for scalars reduced mod r */
+int msm_g1_window_count(int c);                      /* ceil(255 / c): signed windows for scalars reduced mod r
+                                                        (without the GLV split; with it, ceil(128 / c)) */
 int msm_g1_auto_window(size_t n);                    /* the window the library picks for window_c = 0 */
 size_t msm_g1_scratch_bytes(size_t max_n, int max_c); /* device bytes msm_g1_create allocates */
 const char *msm_g1_strerror(int code);

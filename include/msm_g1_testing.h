@@ -49,11 +49,23 @@ int msm_g1_test_batch_add(const uint32_t *a, const uint32_t *b, uint32_t *out, s
                           cudaStream_t stream);
 
 /* Signed window digits of n scalars (8 uint32 each) as the MSM forms them:
- * digits (n x W int32, W = ceil(255/c), window-major per scalar).  Window w
- * covers bits [off_w, off_w + c_w) with c_w = c for the lowest W - e windows
- * and c - 1 for the top e = W c - 255 ones; each digit lies in
- * (-2^(c_w - 1), 2^(c_w - 1)] and sum_w digit_w 2^off_w = k mod r. */
-int msm_g1_test_digits(const uint32_t *scalars, size_t n, int c, int32_t *digits, cudaStream_t stream);
+ * digits (n x W int32, W = ceil(nbits/c), window-major per scalar), nbits =
+ * 255 for scalars reduced mod r (plain windows) or 128 for GLV halves (the
+ * scalars must then be < 2^127).  With q = floor(nbits/W) and e = nbits - q W,
+ * window w covers bits [off_w, off_w + c_w), c_w = q + 1 for the lowest e
+ * windows and q for the others; each digit lies in (-2^(c_w - 1), 2^(c_w - 1)]
+ * and sum_w digit_w 2^off_w = k (k mod r for nbits = 255). */
+int msm_g1_test_digits(const uint32_t *scalars, size_t n, int c, int nbits, int32_t *digits, cudaStream_t stream);
+
+/* GLV split of n scalars (8 uint32 each, reduced mod r first): out holds 10
+ * uint32 per scalar, |k1| (4 limbs), |k2| (4 limbs), then the signs s1, s2
+ * (1 = negative), with k = k1 + lambda k2 (mod r) and |k1|, |k2| < 2^127. */
+int msm_g1_test_glv_split(const uint32_t *scalars, size_t n, uint32_t *out, cudaStream_t stream);
+
+/* Host-only: the endomorphism constants the device code uses, beta in
+ * Montgomery form (8 limbs; phi(x, y) = (beta x, y)) and lambda (8 limbs,
+ * plain, phi = [lambda] on G1).  Touches no device. */
+int msm_g1_glv_constants(uint32_t *beta_mont, uint32_t *lambda);
 
 /* Copy an internal buffer of the last run to host memory (synchronises):
  * which = 0: bucket counts (W*B uint32), 1: even-padded bucket offsets

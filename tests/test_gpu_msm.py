@@ -28,11 +28,12 @@ def ctx(max_n, max_c):
     return _ctx[key]
 
 
-def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=32, tpb=128):
+def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=32, tpb=128, glv=1):
     n = k.shape[0]
     cx = ctx(max_n or max(n, 1), max_c or max(c, 1))
     cx.set_param(gm.PARAM_BATCH_S, batch_s)
     cx.set_param(gm.PARAM_TPB, tpb)
+    cx.set_param(gm.PARAM_GLV, glv)
     out = cx.run(gpu_points(points_affine), gpu_scalars(k), c)
     res = normalise(out)
     assert cx.stats()["error"] == 0
@@ -43,29 +44,32 @@ def expect_oracle(points_affine, k):
     return oracle.msm(points_affine, k)
 
 
-def test_config1_n1024_c8():
+@pytest.mark.parametrize("glv", [1, 0])
+def test_config1_n1024_c8(glv):
     """n = 2^10, c = 8, uniform points [r_i]G and scalars (seed 1001)."""
     r, k = synth.uniform_workload(1 << 10, 1001)
     pts = points_from_r(r)
-    got = run_gpu(pts, k, 8)
+    got = run_gpu(pts, k, 8, glv=glv)
     assert np.array_equal(got, expect_oracle(pts, k))
     assert np.array_equal(got, oracle.closed_form(r, k))
     assert oracle.is_on_curve(got)
 
 
+@pytest.mark.parametrize("glv", [1, 0])
 @pytest.mark.parametrize("n,c", [(1, 4), (2, 3), (3, 8), (7, 5), (31, 6), (33, 7), (100, 9),
                                  (257, 10), (1000, 11), (4097, 12)])
-def test_small_sizes(n, c):
+def test_small_sizes(n, c, glv):
     r, k = synth.uniform_workload(n, 2000 + n)
     pts = points_from_r(r)
-    assert np.array_equal(run_gpu(pts, k, c), expect_oracle(pts, k))
+    assert np.array_equal(run_gpu(pts, k, c, glv=glv), expect_oracle(pts, k))
 
 
+@pytest.mark.parametrize("glv", [1, 0])
 @pytest.mark.parametrize("c", list(range(1, 21)))
-def test_every_window_size(c):
+def test_every_window_size(c, glv):
     r, k = synth.uniform_workload(1500, 3000 + c)
     pts = points_from_r(r)
-    assert np.array_equal(run_gpu(pts, k, c, max_n=1500, max_c=20), expect_oracle(pts, k))
+    assert np.array_equal(run_gpu(pts, k, c, max_n=1500, max_c=20, glv=glv), expect_oracle(pts, k))
 
 
 @pytest.fixture(scope="module")
@@ -126,11 +130,34 @@ def test_empty_input():
     assert oracle.words_to_point(normalise(out)) is None
 
 
-@pytest.mark.parametrize("kval", [0, 1, 2, 3, pyref.R - 1, pyref.R, pyref.R + 1, (1 << 256) - 1, 1 << 255])
-def test_single_term(kval):
+LAMBDA = 0xb3c4d79d41a917585bfc41088d8daaa78b17ea66b99c90dd  # the endomorphism's eigenvalue (pinned in test_glv)
+
+
+@pytest.mark.parametrize("glv", [1, 0])
+@pytest.mark.parametrize("kval", [0, 1, 2, 3, pyref.R - 1, pyref.R, pyref.R + 1, (1 << 256) - 1, 1 << 255,
+                                  LAMBDA, pyref.R - LAMBDA, LAMBDA * LAMBDA % pyref.R, (1 << 127) - 1, 1 << 127])
+def test_single_term(kval, glv):
+    """One term, including scalars whose GLV halves are zero, one or negative."""
     pts = points_from_r(oracle.ints_to_limbs([987654321]))
     k = oracle.ints_to_limbs([kval])
-    assert np.array_equal(run_gpu(pts, k, 8, max_n=16, max_c=8), expect_oracle(pts, k))
+    assert np.array_equal(run_gpu(pts, k, 8, max_n=16, max_c=8, glv=glv), expect_oracle(pts, k))
+
+
+@pytest.mark.parametrize("c", [4, 8])
+def test_glv_images_collide_with_inputs(c):
+    """Inputs P, phi(P) = [lambda]P and -phi(P), all with one scalar k: in the
+    GLV path every bucket then holds copies of P, phi(P), -phi(P) and
+    phi(phi(P)), so the accumulation meets doublings (equal points), P == -Q
+    cancellations and, where a window's two digits coincide, the sum
+    P + phi(P) + phi^2(P) = [1 + lambda + lambda^2]P = infinity."""
+    assert LAMBDA == gm.glv_constants()[1]
+    t = 424242
+    r = [t] * 300 + [t * LAMBDA % pyref.R] * 300 + [(pyref.R - t) * LAMBDA % pyref.R] * 150
+    kk = synth.limbs_to_ints(synth.uniform_workload(1, 62)[1])[0]
+    k = oracle.ints_to_limbs([kk] * len(r))
+    pts = points_from_r(oracle.ints_to_limbs(r))
+    # max_n = 2 x 750 so that c = 4 (2n x 32 entries) fits the context
+    assert np.array_equal(run_gpu(pts, k, c, max_n=1500, max_c=8), expect_oracle(pts, k))
 
 
 def test_all_zero_scalars():
@@ -174,14 +201,15 @@ def test_progression_points(scal):
     assert np.array_equal(run_gpu(pts, k, 7), expect_oracle(pts, k))
 
 
+@pytest.mark.parametrize("glv", [1, 0])
 @pytest.mark.parametrize("finish_t", [1, 8])
-def test_adversarial_small(finish_t):
+def test_adversarial_small(finish_t, glv):
     r, k = synth.adversarial_workload(30000, 1005)
     pts = points_from_r(r)
     cx = ctx(30000, 16)
     cx.set_param(gm.PARAM_FINISH, finish_t)
     try:
-        got = run_gpu(pts, k, 12, max_n=30000, max_c=16)
+        got = run_gpu(pts, k, 12, max_n=30000, max_c=16, glv=glv)
     finally:
         cx.set_param(gm.PARAM_FINISH, 0)
     assert np.array_equal(got, expect_oracle(pts, k))
@@ -195,23 +223,36 @@ def test_deterministic_result():
     assert np.array_equal(a, b)
 
 
-def test_sort_structure():
+@pytest.mark.parametrize("glv", [0, 1])
+def test_sort_structure(glv):
     """The sorted bucket list: every entry sits in the bucket of its digit,
-    with the right negate flag; odd buckets carry one padding entry."""
+    with the right negate flag; odd buckets carry one padding entry.  With
+    GLV, entries i < n carry the digits of |k1_i| (negated when k1_i < 0) and
+    entries n + i those of |k2_i| on phi(P_i)."""
     n, c = 3000, 9
     r, k = synth.uniform_workload(n, 99)
     pts = points_from_r(r)
     cx = ctx(n, c)
     cx.set_param(gm.PARAM_BATCH_S, 8)
+    cx.set_param(gm.PARAM_GLV, glv)
     torch.cuda.synchronize()
     cx.run(gpu_points(pts), gpu_scalars(k), c)
-    W, B = gm.window_count(c), 1 << (c - 1)
+    B = 1 << (c - 1)
+    if glv:
+        halves = gm.to_host(gm.test_glv_split(gpu_scalars(k))).reshape(n, 10)
+        words = np.zeros((2 * n, 8), dtype=np.uint32)
+        words[:n, :4], words[n:, :4] = halves[:, 0:4], halves[:, 4:8]
+        digits = gm.to_host(gm.test_digits(gm.to_device(words), c, gm.GLV_BITS)).view(np.int32)
+        flip = np.concatenate([halves[:, 8], halves[:, 9]]).astype(bool)
+    else:
+        digits = gm.to_host(gm.test_digits(gpu_scalars(k), c)).view(np.int32)
+        flip = np.zeros(n, dtype=bool)
+    W = digits.shape[1]
     counts, _ = cx.debug_read(0, W * B)
     offsets, _ = cx.debug_read(1, W * B + 1)
     total = int(offsets[-1])
     entries, nbytes = cx.debug_read(2, total)
     assert nbytes == 4 * total
-    digits = gm.to_host(gm.test_digits(gpu_scalars(k), c)).view(np.int32)
     expect_count = np.zeros(W * B, dtype=np.int64)
     for w in range(W):
         d = digits[:, w]
@@ -227,10 +268,11 @@ def test_sort_structure():
         idx = seg & 0x7FFFFFFF
         neg = (seg >> 31) == 1
         dig = digits[idx, w]
-        assert np.all(np.abs(dig) == b + 1) and np.all((dig < 0) == neg)
+        assert np.all(np.abs(dig) == b + 1) and np.all(((dig < 0) ^ flip[idx]) == neg)
         assert len(set(idx.tolist())) == m
         if m & 1:
             assert entries[o + m] == 0xFFFFFFFF
+    cx.set_param(gm.PARAM_GLV, 1)
 
 
 def test_capacity_and_argument_errors():
@@ -272,12 +314,13 @@ def big_points():
     return r, points_from_r(r)
 
 
-def test_config2_n65536_c13(big_points):
+@pytest.mark.parametrize("glv", [1, 0])
+def test_config2_n65536_c13(big_points, glv):
     r_all, pts_all = big_points
     n = 1 << 16
     _, k = synth.uniform_workload(n, 1002)
     r, pts = r_all[:n], pts_all[:n]
-    got = run_gpu(pts, k, 13, max_n=n, max_c=13)
+    got = run_gpu(pts, k, 13, max_n=n, max_c=13, glv=glv)
     assert np.array_equal(got, expect_oracle(pts, k))
     assert np.array_equal(got, oracle.closed_form(r, k))
 
@@ -291,17 +334,18 @@ def test_config3_n2p20_c16(big_points, batch_s):
     assert np.array_equal(got, oracle.closed_form(r_all[:n], k))
 
 
-@pytest.mark.parametrize("c", [16, 17, 18])
-def test_config4_n2p22(big_points, c):
+@pytest.mark.parametrize("c,glv", [(16, 1), (17, 1), (18, 1), (16, 0)])
+def test_config4_n2p22(big_points, c, glv):
     r, pts = big_points
     _, k = synth.uniform_workload(1 << 22, 1005)
-    got = run_gpu(pts, k, c, max_n=1 << 22, max_c=18)
+    got = run_gpu(pts, k, c, max_n=1 << 22, max_c=18, glv=glv)
     assert np.array_equal(got, oracle.closed_form(r, k))
 
 
-def test_config5_adversarial_n2p20():
+@pytest.mark.parametrize("glv", [1, 0])
+def test_config5_adversarial_n2p20(glv):
     n = 1 << 20
     r, k = synth.adversarial_workload(n, 1006)
     pts = points_from_r(r)
-    got = run_gpu(pts, k, 16, max_n=n, max_c=16)
+    got = run_gpu(pts, k, 16, max_n=n, max_c=16, glv=glv)
     assert np.array_equal(got, oracle.closed_form(r, k))

@@ -111,24 +111,61 @@ def test_batch_affine_add(batch_s):
         assert aff_words_to_point(out[i]) == pyref.add(p, q), (batch_s, i)
 
 
-def window_layout(c):
-    """Widths of the W = ceil(255 / c) windows: the top W c - 255 are c - 1 bits."""
-    W = -(-255 // c)
-    narrow = W * c - 255
-    return [c - 1 if w >= W - narrow else c for w in range(W)]
+def window_layout(c, nbits):
+    """Widths of the W = ceil(nbits / c) windows, balanced: the low
+    nbits - W floor(nbits / W) windows are one bit wider than the rest."""
+    W = -(-nbits // c)
+    q = nbits // W
+    wide = nbits - q * W
+    return [q + 1 if w < wide else q for w in range(W)]
 
 
+def test_window_layout_reduces_to_c_and_c_minus_1_for_full_scalars():
+    """For 255 bits the balanced layout is c-bit windows with the top
+    W c - 255 one bit narrower."""
+    for c in range(1, 21):
+        W = -(-255 // c)
+        narrow = W * c - 255
+        if narrow <= W:
+            assert window_layout(c, 255) == [c - 1 if w >= W - narrow else c for w in range(W)]
+
+
+@pytest.mark.parametrize("nbits", [255, 128])
 @pytest.mark.parametrize("c", [1, 2, 5, 8, 13, 16, 17, 18, 20])
-def test_signed_digits(c):
+def test_signed_digits(c, nbits):
     rng = random.Random(c)
-    ks = [0, 1, R - 1, R, R + 1, (1 << 256) - 1, (1 << 254), 2 ** (c - 1), 2 ** c - 1]
-    ks += [rng.randrange(0, 1 << 256) for _ in range(300)]
-    d = gm.test_digits(gm.to_device(ints_to_u32(ks)), c)
+    if nbits == 255:
+        ks = [0, 1, R - 1, R, R + 1, (1 << 256) - 1, (1 << 254), 2 ** (c - 1), 2 ** c - 1]
+        ks += [rng.randrange(0, 1 << 256) for _ in range(300)]
+    else:  # GLV halves, < 2^127
+        ks = [0, 1, (1 << 127) - 1, 1 << 126, 2 ** (c - 1), 2 ** c - 1, ((1 << 127) - 1) // 3]
+        ks += [rng.randrange(0, 1 << 127) for _ in range(300)]
+    d = gm.test_digits(gm.to_device(ints_to_u32(ks)), c, nbits)
     digits = gm.to_host(d).view(np.int32)
-    widths = window_layout(c)
-    W = gm.window_count(c)
-    assert digits.shape == (len(ks), W) and len(widths) == W and sum(widths) == 255
+    widths = window_layout(c, nbits)
+    W = -(-nbits // c)
+    if nbits == 255:
+        assert W == gm.window_count(c)
+    assert digits.shape == (len(ks), W) and len(widths) == W and sum(widths) == nbits and max(widths) <= c
     offsets = [sum(widths[:w]) for w in range(W)]
     for k, row in zip(ks, digits):
         assert all(-(1 << (cw - 1)) < int(v) <= (1 << (cw - 1)) for v, cw in zip(row, widths))
         assert sum(int(v) << off for v, off in zip(row, offsets)) == k % R
+
+
+def test_glv_split_on_device():
+    """The device split k -> (k1, k2): k = k1 + lambda k2 (mod r) and
+    |k1|, |k2| < 2^127, for reduced and unreduced scalars."""
+    _, lam = gm.glv_constants()
+    rng = random.Random(11)
+    ks = [0, 1, 2, R - 1, R, R + 1, lam, R - lam, (1 << 256) - 1, 1 << 127, (R - 1) // 2]
+    ks += [rng.randrange(0, 1 << 256) for _ in range(5000)]
+    out = gm.to_host(gm.test_glv_split(gm.to_device(ints_to_u32(ks)))).reshape(-1, 10)
+    for k, row in zip(ks, out):
+        a = sum(int(v) << (32 * j) for j, v in enumerate(row[0:4]))
+        b = sum(int(v) << (32 * j) for j, v in enumerate(row[4:8]))
+        assert int(row[8]) in (0, 1) and int(row[9]) in (0, 1)
+        k1 = -a if row[8] else a
+        k2 = -b if row[9] else b
+        assert a < 1 << 127 and b < 1 << 127
+        assert (k1 + lam * k2 - k) % R == 0, k
