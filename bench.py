@@ -43,13 +43,16 @@ CONFIGS = {
 PAGES_MS_LOGN16 = 50.0
 
 # IMAD roofline.  Each SM issues 64 low-half 32-bit multiply-adds per clock
-# (4 sub-partitions x 16 lanes) and the high-half form at half that rate
-# (measured on this GB300: mad.lo 18.7 Tops/s, mad.hi 8.7 Tops/s).  A
-# Montgomery multiplication on 8 x 32-bit limbs issues 64 + 64 low products
-# (a_i b_j, m_i p_j), 8 low products m_i = t_i n', and 64 + 64 high products,
-# i.e. 136 + 2 * 128 = 392 low-multiply issue slots.
+# (4 sub-partitions x 16 lanes); a full 32 x 32 -> 64-bit limb product (a
+# lo/hi pair over the same operands in one carry chain, which issues as one
+# 64-bit multiply-add) takes two of those slots (measured on this GB300 by
+# elliptic_curve_scalar_gb300/csrc/imad_rate.cu: mad.lo 18.7 Tops/s, paired
+# lo/hi rows 8.9 T products/s).  A Montgomery multiplication on 8 x 32-bit
+# limbs needs 64 + 64 full products (a_i b_j, m_i p_j) and 8 low products
+# m_i = t_i n': 2 * 128 + 8 = 264 slots, the fewest any schoolbook
+# Montgomery multiplication can issue on this pipe.
 IMAD_SLOTS_PER_CLK_PER_SM = 64
-IMAD_SLOTS_PER_FQ_MUL = 136 + 2 * 128
+IMAD_SLOTS_PER_FQ_MUL = 2 * 128 + 8
 FQ_MULS_PER_ADD = 6  # 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
 
 
@@ -334,7 +337,7 @@ def run_gpu(args, cfg):
                          "kernel": "k_accum_level0",
                          "peak_basis": "%d SMs x %d IMAD slots/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
                                        % (sms, IMAD_SLOTS_PER_CLK_PER_SM, sm_max_mhz),
-                         "count_basis": "6 Fq muls per addition x 392 IMAD slots per mul (inversion excluded)",
+                         "count_basis": "6 Fq muls per addition x 264 IMAD slots per mul (128 full limb products at 2 slots + 8 low; inversion excluded)",
                          "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
                          "inversion": "safegcd (Bernstein-Yang divsteps), one per %d additions" % args.batch_s,

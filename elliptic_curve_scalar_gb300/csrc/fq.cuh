@@ -11,11 +11,13 @@
 //
 // Multiplication is Montgomery's REDC on the full product (separated operand
 // scanning, see mul below).  Every carry chain sits in a single asm statement
-// so that nothing can clobber the carry flag inside it.  On this part the
-// multiply-high form of the 32-bit multiply-add issues at half the rate of
-// the low form, so a multiplication (136 low + 128 high products) costs about
-// 392 low-multiply issue slots; that mix is the roofline the kernels are
-// measured against.
+// so that nothing can clobber the carry flag inside it.  On this part a lone
+// 32-bit multiply-add issues in one slot of the multiply pipe for the low half
+// and two for the high half, but a lo/hi pair over the same operands in one
+// carry chain issues as one 64-bit multiply-add in two slots.  Every one of
+// the 128 limb products of a multiplication is such a pair and the 8 reduction
+// factors m are low-only, so a multiplication needs 264 slots: the roofline
+// the kernels are measured against.
 #pragma once
 #include <stdint.h>
 
@@ -150,95 +152,74 @@ __device__ __forceinline__ fe neg(const fe& a) {
 
 __device__ __forceinline__ fe dbl(const fe& a) { return add(a, a); }
 
-// Row of partial products a_i * (b_0, b_2, b_4, b_6) (or the odd limbs of b)
-// added into t[0..7] as lo, hi, lo, hi, ...: one unbroken carry chain, with the
-// carry out added into t[8].
-__device__ __forceinline__ void mac_row4(uint32_t* t, uint32_t ai, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-    asm("mad.lo.cc.u32  %0, %9, %10, %0;\n\t"
-        "madc.hi.cc.u32 %1, %9, %10, %1;\n\t"
-        "madc.lo.cc.u32 %2, %9, %11, %2;\n\t"
-        "madc.hi.cc.u32 %3, %9, %11, %3;\n\t"
-        "madc.lo.cc.u32 %4, %9, %12, %4;\n\t"
-        "madc.hi.cc.u32 %5, %9, %12, %5;\n\t"
-        "madc.lo.cc.u32 %6, %9, %13, %6;\n\t"
-        "madc.hi.cc.u32 %7, %9, %13, %7;\n\t"
-        "addc.u32       %8, %8, 0;"
-        : "+r"(t[0]), "+r"(t[1]), "+r"(t[2]), "+r"(t[3]), "+r"(t[4]), "+r"(t[5]), "+r"(t[6]), "+r"(t[7]), "+r"(t[8])
-        : "r"(ai), "r"(b0), "r"(b1), "r"(b2), "r"(b3));
+// Multiply-accumulate of one row, T[0..8] += x * (y_0 .. y_7), with the carry
+// out of T[8] returned in cin (which holds, on entry, a carry to add into
+// T[8]).  Each partial product is a lo/hi pair over the same operands written
+// to adjacent limbs inside one carry chain (mad.lo.cc then madc.hi.cc): the
+// compiler issues such a pair as a single 64-bit multiply-add, two issue
+// slots of the multiply pipe instead of three for an unpaired lo and hi.  The
+// even products y_0, y_2, y_4, y_6 fill limbs (0,1), (2,3), (4,5), (6,7) in
+// one chain, the odd ones limbs (1,2) .. (7,8) in a second.
+#define FQ_ROW_ASM                                \
+    "{\n\t.reg .u32 c1;\n\t"                      \
+    "mad.lo.cc.u32  %0, %10, %11, %0;\n\t"        \
+    "madc.hi.cc.u32 %1, %10, %11, %1;\n\t"        \
+    "madc.lo.cc.u32 %2, %10, %13, %2;\n\t"        \
+    "madc.hi.cc.u32 %3, %10, %13, %3;\n\t"        \
+    "madc.lo.cc.u32 %4, %10, %15, %4;\n\t"        \
+    "madc.hi.cc.u32 %5, %10, %15, %5;\n\t"        \
+    "madc.lo.cc.u32 %6, %10, %17, %6;\n\t"        \
+    "madc.hi.cc.u32 %7, %10, %17, %7;\n\t"        \
+    "addc.cc.u32    %8, %8, %9;\n\t"              \
+    "addc.u32       c1, 0, 0;\n\t"                \
+    "mad.lo.cc.u32  %1, %10, %12, %1;\n\t"        \
+    "madc.hi.cc.u32 %2, %10, %12, %2;\n\t"        \
+    "madc.lo.cc.u32 %3, %10, %14, %3;\n\t"        \
+    "madc.hi.cc.u32 %4, %10, %14, %4;\n\t"        \
+    "madc.lo.cc.u32 %5, %10, %16, %5;\n\t"        \
+    "madc.hi.cc.u32 %6, %10, %16, %6;\n\t"        \
+    "madc.lo.cc.u32 %7, %10, %18, %7;\n\t"        \
+    "madc.hi.cc.u32 %8, %10, %18, %8;\n\t"        \
+    "addc.u32       %9, c1, 0;\n\t"               \
+    "}"
+#define FQ_ROW_OUT(T, cin) \
+    "+r"((T)[0]), "+r"((T)[1]), "+r"((T)[2]), "+r"((T)[3]), "+r"((T)[4]), "+r"((T)[5]), "+r"((T)[6]), "+r"((T)[7]), \
+        "+r"((T)[8]), "+r"(cin)
+
+__device__ __forceinline__ void mac_row(uint32_t* T, uint32_t& cin, uint32_t x, const uint32_t (&y)[8]) {
+    asm(FQ_ROW_ASM
+        : FQ_ROW_OUT(T, cin)
+        : "r"(x), "r"(y[0]), "r"(y[1]), "r"(y[2]), "r"(y[3]), "r"(y[4]), "r"(y[5]), "r"(y[6]), "r"(y[7]));
 }
 
-// a * b * R^-1 mod p by separated operand scanning.  The 512-bit product is
-// built in two independent accumulators -- E for the even limbs of b, O for
-// the odd ones, one limb higher -- so that the two carry chains of each row
-// can overlap; E + O is then reduced by eight Montgomery rounds
-// t += m p 2^(32 i), m = t_i (-p^-1) mod 2^32.  A round's carry out of limb
-// i+8 belongs to limb i+9 and is added in the next round's chain.  T stays
-// below p^2 + p R < 2^511, and T / R < 2p needs one conditional subtraction.
+// the same row with y = p (immediate operands)
+__device__ __forceinline__ void mac_row_p(uint32_t* T, uint32_t& cin, uint32_t m) {
+    asm(FQ_ROW_ASM
+        : FQ_ROW_OUT(T, cin)
+        : "r"(m), "n"(FQ_P0), "n"(FQ_P1), "n"(FQ_P2), "n"(FQ_P3), "n"(FQ_P4), "n"(FQ_P5), "n"(FQ_P6), "n"(FQ_P7));
+}
+
+// a * b * R^-1 mod p by separated operand scanning: the 512-bit product
+// T = a b row by row (row i adds a_i b at limb i; its carry out of limb i+8
+// starts limb i+9), then eight Montgomery rounds T += m p 2^(32 i) with
+// m = T_i (-p^-1) mod 2^32, each of which zeroes limb i.  A round's carry out
+// of limb i+8 belongs to limb i+9 and enters the next round's chain there.
+// T stays below p^2 + p R < 2^511, so limb 16 and the last carry are zero, and
+// T / R < 2p needs one conditional subtraction.
 __device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
-    uint32_t E[17], O[17];
-#pragma unroll
-    for (int i = 0; i < 17; i++) {
-        E[i] = 0;
-        O[i] = 0;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        mac_row4(E + i, a.v[i], b.v[0], b.v[2], b.v[4], b.v[6]);
-        mac_row4(O + i + 1, a.v[i], b.v[1], b.v[3], b.v[5], b.v[7]);
-    }
     uint32_t T[17];
-    asm("add.cc.u32  %0, %17, %34;\n\t"
-        "addc.cc.u32 %1, %18, %35;\n\t"
-        "addc.cc.u32 %2, %19, %36;\n\t"
-        "addc.cc.u32 %3, %20, %37;\n\t"
-        "addc.cc.u32 %4, %21, %38;\n\t"
-        "addc.cc.u32 %5, %22, %39;\n\t"
-        "addc.cc.u32 %6, %23, %40;\n\t"
-        "addc.cc.u32 %7, %24, %41;\n\t"
-        "addc.cc.u32 %8, %25, %42;\n\t"
-        "addc.cc.u32 %9, %26, %43;\n\t"
-        "addc.cc.u32 %10, %27, %44;\n\t"
-        "addc.cc.u32 %11, %28, %45;\n\t"
-        "addc.cc.u32 %12, %29, %46;\n\t"
-        "addc.cc.u32 %13, %30, %47;\n\t"
-        "addc.cc.u32 %14, %31, %48;\n\t"
-        "addc.cc.u32 %15, %32, %49;\n\t"
-        "addc.u32    %16, %33, %50;"
-        : "=r"(T[0]), "=r"(T[1]), "=r"(T[2]), "=r"(T[3]), "=r"(T[4]), "=r"(T[5]), "=r"(T[6]), "=r"(T[7]), "=r"(T[8]),
-          "=r"(T[9]), "=r"(T[10]), "=r"(T[11]), "=r"(T[12]), "=r"(T[13]), "=r"(T[14]), "=r"(T[15]), "=r"(T[16])
-        : "r"(E[0]), "r"(E[1]), "r"(E[2]), "r"(E[3]), "r"(E[4]), "r"(E[5]), "r"(E[6]), "r"(E[7]), "r"(E[8]),
-          "r"(E[9]), "r"(E[10]), "r"(E[11]), "r"(E[12]), "r"(E[13]), "r"(E[14]), "r"(E[15]), "r"(E[16]),
-          "r"(O[0]), "r"(O[1]), "r"(O[2]), "r"(O[3]), "r"(O[4]), "r"(O[5]), "r"(O[6]), "r"(O[7]), "r"(O[8]),
-          "r"(O[9]), "r"(O[10]), "r"(O[11]), "r"(O[12]), "r"(O[13]), "r"(O[14]), "r"(O[15]), "r"(O[16]));
-    uint32_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 17; i++) T[i] = 0;
+    uint32_t cin;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-        uint32_t m = T[i] * FQ_NP0;
-        asm("{\n\t.reg .u32 c;\n\t"
-            "mad.lo.cc.u32  %0, %10, %11, %0;\n\t"
-            "madc.lo.cc.u32 %1, %10, %12, %1;\n\t"
-            "madc.lo.cc.u32 %2, %10, %13, %2;\n\t"
-            "madc.lo.cc.u32 %3, %10, %14, %3;\n\t"
-            "madc.lo.cc.u32 %4, %10, %15, %4;\n\t"
-            "madc.lo.cc.u32 %5, %10, %16, %5;\n\t"
-            "madc.lo.cc.u32 %6, %10, %17, %6;\n\t"
-            "madc.lo.cc.u32 %7, %10, %18, %7;\n\t"
-            "addc.cc.u32    %8, %8, %9;\n\t"
-            "addc.u32       c, 0, 0;\n\t"
-            "mad.hi.cc.u32  %1, %10, %11, %1;\n\t"
-            "madc.hi.cc.u32 %2, %10, %12, %2;\n\t"
-            "madc.hi.cc.u32 %3, %10, %13, %3;\n\t"
-            "madc.hi.cc.u32 %4, %10, %14, %4;\n\t"
-            "madc.hi.cc.u32 %5, %10, %15, %5;\n\t"
-            "madc.hi.cc.u32 %6, %10, %16, %6;\n\t"
-            "madc.hi.cc.u32 %7, %10, %17, %7;\n\t"
-            "madc.hi.cc.u32 %8, %10, %18, %8;\n\t"
-            "addc.u32       %9, c, 0;\n\t"
-            "}"
-            : "+r"(T[i]), "+r"(T[i + 1]), "+r"(T[i + 2]), "+r"(T[i + 3]), "+r"(T[i + 4]), "+r"(T[i + 5]),
-              "+r"(T[i + 6]), "+r"(T[i + 7]), "+r"(T[i + 8]), "+r"(carry)
-            : "r"(m), "n"(FQ_P0), "n"(FQ_P1), "n"(FQ_P2), "n"(FQ_P3), "n"(FQ_P4), "n"(FQ_P5), "n"(FQ_P6), "n"(FQ_P7));
+        cin = 0;
+        mac_row(T + i, cin, a.v[i], b.v);
+        T[i + 9] = cin;
     }
+    cin = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) mac_row_p(T + i, cin, T[i] * FQ_NP0);
     fe r;
 #pragma unroll
     for (int j = 0; j < 8; j++) r.v[j] = T[8 + j];
@@ -250,8 +231,10 @@ __device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
 // multiplications, and inlining each ~330-instruction body at every call site
 // makes the hot loops overflow the per-sub-partition instruction cache (the
 // warps then stall waiting for instruction fetch).  One shared body stays
-// resident.
-static __device__ __noinline__ fe mul(const fe& a, const fe& b) { return mul_inline(a, b); }
+// resident.  The operands are taken by value: a reference parameter of a called function
+// makes the caller store the operand to its stack frame and the callee load it
+// back, two round trips through local memory per multiplication.
+static __device__ __noinline__ fe mul(fe a, fe b) { return mul_inline(a, b); }
 
 __device__ __forceinline__ fe sqr(const fe& a) { return mul(a, a); }
 
@@ -263,7 +246,7 @@ __device__ __forceinline__ fe sqr_n(fe a, int n) {
 // a^(p-2) = a^-1 (Fermat; p prime), inv(0) = 0.  Fixed 4-bit windows over the
 // exponent p - 2, most significant first: 252 squarings and at most 63
 // multiplications by the table entry a^w.
-static __device__ __noinline__ fe inv_fermat(const fe& a) {
+static __device__ __noinline__ fe inv_fermat(fe a) {
     // p - 2 in 4-bit digits, most significant first
     const uint32_t e[8] = {FQ_P7, FQ_P6, FQ_P5, FQ_P4, FQ_P3, FQ_P2, FQ_P1, FQ_P0 - 2u};
     fe tbl[16];

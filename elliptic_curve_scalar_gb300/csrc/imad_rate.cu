@@ -3,8 +3,10 @@
 // bench.py reports.  Standalone program:
 //   nvcc -O3 -std=c++17 -gencode arch=compute_103a,code=sm_103a \
 //        -o imad_rate elliptic_curve_scalar_gb300/csrc/imad_rate.cu && ./imad_rate
-// Prints mad.lo / mad.hi / carry-chained madc throughput (ops/s), dependent
-// latencies (cycles), and fq::mul latency and throughput.
+// Prints mad.lo / mad.hi / carry-chained madc throughput (ops/s), the rate of
+// full limb products issued as lo/hi pairs in one carry chain (the form the
+// field multiplication uses) and as unpaired lo and hi, dependent latencies
+// (cycles), and fq::mul latency and throughput.
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -71,6 +73,38 @@ __global__ void k_madc_tput(uint32_t* out, int iters, uint32_t seed) {
     }
     uint32_t x = 0;
     for (int c = 0; c < 4; c++) for (int j = 0; j < 8; j++) x ^= t[c][j];
+    out[blockIdx.x * blockDim.x + threadIdx.x] = x;
+}
+
+// ---------- full limb products: rows of lo/hi pairs over the same operands
+// (fq::mac_row), two independent rows of 8 products per iteration
+__global__ void k_pair_row_tput(uint32_t* out, int iters, uint32_t seed) {
+    uint32_t t[2][9], cin[2] = {0, 0};
+    for (int c = 0; c < 2; c++) for (int j = 0; j < 9; j++) t[c][j] = seed + c * 9 + j + threadIdx.x;
+    uint32_t b[8];
+    for (int j = 0; j < 8; j++) b[j] = seed * (j + 3) + 1;
+    for (int i = 0; i < iters; i++) {
+#pragma unroll
+        for (int c = 0; c < 2; c++) fq::mac_row(t[c], cin[c], t[c][8] ^ cin[c] ^ (uint32_t)i, b);
+    }
+    uint32_t x = cin[0] ^ cin[1];
+    for (int c = 0; c < 2; c++) for (int j = 0; j < 9; j++) x ^= t[c][j];
+    out[blockIdx.x * blockDim.x + threadIdx.x] = x;
+}
+
+// unpaired: 8 mad.hi and 8 mad.lo on different operands per iteration
+__global__ void k_unpaired_tput(uint32_t* out, int iters, uint32_t seed) {
+    uint32_t h[8], l[8];
+    for (int j = 0; j < 8; j++) { h[j] = seed + threadIdx.x + j; l[j] = h[j] * 7; }
+    for (int i = 0; i < iters; i++) {
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            asm volatile("mad.hi.u32 %0, %0, %1, %0;" : "+r"(h[j]) : "r"(l[j]));
+            asm volatile("mad.lo.u32 %0, %0, %1, %0;" : "+r"(l[j]) : "r"(h[j]));
+        }
+    }
+    uint32_t x = 0;
+    for (int j = 0; j < 8; j++) x ^= h[j] ^ l[j];
     out[blockIdx.x * blockDim.x + threadIdx.x] = x;
 }
 
@@ -166,6 +200,18 @@ int main() {
     CK(cudaEventSynchronize(e1));
     cudaEventElapsedTime(&ms, e0, e1);
     printf("madc.lo.cc chain throughput: %.3f Tops/s\n", (double)blocks * tpb * (iters / 4) * 32 / (ms * 1e-3) / 1e12);
+    cudaEventRecord(e0);
+    k_pair_row_tput<<<blocks, tpb>>>(d_out, iters / 4, 1);
+    cudaEventRecord(e1);
+    CK(cudaEventSynchronize(e1));
+    cudaEventElapsedTime(&ms, e0, e1);
+    printf("paired lo/hi rows: %.3f T full products/s\n", (double)blocks * tpb * (iters / 4) * 16 / (ms * 1e-3) / 1e12);
+    cudaEventRecord(e0);
+    k_unpaired_tput<<<blocks, tpb>>>(d_out, iters, 1);
+    cudaEventRecord(e1);
+    CK(cudaEventSynchronize(e1));
+    cudaEventElapsedTime(&ms, e0, e1);
+    printf("unpaired lo + hi: %.3f T pairs/s\n", (double)blocks * tpb * iters * 8 / (ms * 1e-3) / 1e12);
     k_imad_lat<<<1, 1>>>(d_out, iters, 3, d_cyc);
     CK(cudaMemcpy(&cyc, d_cyc, 8, cudaMemcpyDeviceToHost));
     printf("mad.lo dependent latency: %.2f cycles\n", (double)cyc / (iters * 4));
@@ -183,8 +229,8 @@ int main() {
     CK(cudaEventSynchronize(e1));
     cudaEventElapsedTime(&ms, e0, e1);
     double muls = (double)mb * mt * mit * 2;
-    printf("fq::mul throughput: %.2f Gmul/s = %.2f T IMAD slots/s (392 slots per mul)\n", muls / (ms * 1e-3) / 1e9,
-           muls * 392 / (ms * 1e-3) / 1e12);
+    printf("fq::mul throughput: %.2f Gmul/s = %.2f T IMAD slots/s (264 slots per mul)\n", muls / (ms * 1e-3) / 1e9,
+           muls * 264 / (ms * 1e-3) / 1e12);
     CK(cudaGetLastError());
     return 0;
 }

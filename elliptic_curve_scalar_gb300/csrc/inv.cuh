@@ -178,7 +178,7 @@ __device__ __forceinline__ void add_p_masked(s9& a, int32_t mask) {
 }
 
 // x~ (Montgomery form of x, < p) -> Montgomery form of x^-1; 0 -> 0.
-static __device__ __noinline__ fq::fe inv_safegcd(const fq::fe& xm) {
+static __device__ __noinline__ fq::fe inv_safegcd(fq::fe xm) {
     s9 f, g, d, e;
 #pragma unroll
     for (int i = 0; i < 9; i++) f.v[i] = p30(i);
