@@ -85,7 +85,7 @@ __global__ void k_pair_row_tput(uint32_t* out, int iters, uint32_t seed) {
     for (int j = 0; j < 8; j++) b[j] = seed * (j + 3) + 1;
     for (int i = 0; i < iters; i++) {
 #pragma unroll
-        for (int c = 0; c < 2; c++) fq::mac_row(t[c], cin[c], t[c][8] ^ cin[c] ^ (uint32_t)i, b);
+        for (int c = 0; c < 2; c++) fq::mac_row(t[c], cin[c], (uint32_t)i * 0x9e3779b9u + (uint32_t)c, b);
     }
     uint32_t x = cin[0] ^ cin[1];
     for (int c = 0; c < 2; c++) for (int j = 0; j < 9; j++) x ^= t[c][j];

@@ -74,12 +74,21 @@ struct Level0Src {
     __device__ __forceinline__ void store(int k, const aff& r) { g1::store_aff(items + (size_t)(u0 + k) * 16, r); }
 };
 
+// Each accumulation kernel comes in two builds of one body: at its natural
+// register count (about 100), and capped at 80 registers ("wide": 6 blocks of
+// 128 threads per SM instead of 4, for a few spilled words).  The wide build
+// is used when a launch has at least a resident wave of work, where the extra
+// warps hide latency (n = 2^22 on GB300: 14.17 -> 13.29 ms per MSM; caps of
+// 96, 88, 72 and 64 were slower); small launches are latency-bound and the
+// spills only add latency there (n = 2^16: 1.27 vs 1.32 ms).
+#define LEVEL0_PARAMS                                                                                     \
+    const uint32_t *__restrict__ points, const uint32_t *__restrict__ phi, uint32_t nsplit,                \
+        const uint32_t *__restrict__ entries, const uint32_t *__restrict__ offsets, uint32_t g0, uint32_t g1, \
+        uint32_t *__restrict__ items, ctl_t *ctl, int stats
+#define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats
+
 template <int S>
-__global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict__ points,
-                                                      const uint32_t* __restrict__ phi, uint32_t nsplit,
-                                                      const uint32_t* __restrict__ entries,
-                                                      const uint32_t* __restrict__ offsets, uint32_t g0, uint32_t g1,
-                                                      uint32_t* __restrict__ items, ctl_t* ctl, int stats) {
+__device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     // units of buckets [g0, g1): pairs (2u, 2u+1) for u in [offset_g0 / 2, offset_g1 / 2)
     const uint32_t ubeg = offsets[g0] >> 1;
     const uint32_t units = (offsets[g1] >> 1) - ubeg;
@@ -102,6 +111,15 @@ __global__ void __launch_bounds__(256) k_accum_level0(const uint32_t* __restrict
     }
     int adds = batch_pairs<S>(src, count);
     if (stats) warp_stats(ctl, adds, 1);
+}
+
+template <int S>
+__global__ void __launch_bounds__(256) k_accum_level0(LEVEL0_PARAMS) {
+    accum_level0<S>(LEVEL0_ARGS);
+}
+template <int S>
+__global__ void __maxnreg__(80) k_accum_level0_wide(LEVEL0_PARAMS) {
+    accum_level0<S>(LEVEL0_ARGS);
 }
 
 // ------------------------------------------------------- pair lists per level
@@ -197,8 +215,8 @@ struct ListSrc {
 };
 
 template <int S>
-__global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                    ctl_t* ctl, int grp, int level, int stats) {
+__device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
+                                           ctl_t* ctl, int grp, int level, int stats) {
     const uint32_t cnt = ctl->pair_count[grp][level];
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
@@ -215,6 +233,17 @@ __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items
         warp_stats(ctl, adds, 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
     }
+}
+
+template <int S>
+__global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
+                                                    ctl_t* ctl, int grp, int level, int stats) {
+    accum_list<S>(items, list, ctl, grp, level, stats);
+}
+template <int S>
+__global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
+                                                  ctl_t* ctl, int grp, int level, int stats) {
+    accum_list<S>(items, list, ctl, grp, level, stats);
 }
 
 // ------------------------------------------------------------ small buckets
@@ -249,25 +278,34 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
     return (unsigned)std::max<uint64_t>(1, (threads + tpb - 1) / tpb);
 }
 
+// the register-capped build once the work fills a resident wave of the other
+static bool wide(uint64_t work, int S, const Resident& res) { return (work + S - 1) / S >= res.narrow; }
+
 template <int S>
-static void level0_t(int tpb, uint64_t resident, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
+static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
                      const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
                      ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
-    k_accum_level0<S><<<grid_for(units_ub, S, tpb, resident), tpb, 0, st>>>(points, phi, nsplit, entries, offsets, g0,
-                                                                           g1, items, ctl, stats);
+    if (wide(units_ub, S, res))
+        k_accum_level0_wide<S><<<grid_for(units_ub, S, tpb, res.wide), tpb, 0, st>>>(points, phi, nsplit, entries,
+                                                                                    offsets, g0, g1, items, ctl, stats);
+    else
+        k_accum_level0<S><<<grid_for(units_ub, S, tpb, res.narrow), tpb, 0, st>>>(points, phi, nsplit, entries,
+                                                                                 offsets, g0, g1, items, ctl, stats);
 }
 
 template <int S>
-static void list_t(int tpb, uint64_t resident, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
+static void list_t(int tpb, const Resident& res, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
                    int grp, int level, int stats, cudaStream_t st) {
-    k_accum_list<S><<<grid_for(cap, S, tpb, resident), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
+    if (wide(cap, S, res))
+        k_accum_list_wide<S><<<grid_for(cap, S, tpb, res.wide), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
+    else
+        k_accum_list<S><<<grid_for(cap, S, tpb, res.narrow), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
 }
 
-void launch_accum_level0(int batch_s, int tpb, uint64_t resident, const uint32_t* points, const uint32_t* phi,
+void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi,
                          uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
                          uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
-#define L0(S) \
-    level0_t<S>(tpb, resident, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
+#define L0(S) level0_t<S>(tpb, res, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
     switch (batch_s) {
         case 1: L0(1); break;
         case 2: L0(2); break;
@@ -284,11 +322,11 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
     k_build_pairs<<<(nb + 255) / 256, 256, 0, st>>>(offsets, nb, pairs, lay, ctl);
 }
 
-void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items, const uint32_t* pairs,
+void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* items, const uint32_t* pairs,
                         const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st) {
     const uint32_t* list = pairs + lay.base[grp][level];
     uint64_t cap = lay.cap[grp][level];
-#define LV(S) list_t<S>(tpb, resident, items, list, ctl, cap, grp, level, stats, st)
+#define LV(S) list_t<S>(tpb, res, items, list, ctl, cap, grp, level, stats, st)
     switch (batch_s) {
         case 1: LV(1); break;
         case 2: LV(2); break;
@@ -304,13 +342,18 @@ void launch_accum_level(int batch_s, int tpb, uint64_t resident, uint32_t* items
 
 namespace msm {
 
-uint64_t accum_resident_threads(int tpb) {
-    int dev = 0, sms = 0, b0 = 0, b1 = 0;
+Resident accum_resident_threads(int tpb) {
+    int dev = 0, sms = 0, b0 = 0, b1 = 0, w0 = 0, w1 = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_accum_level0<32>, tpb, 0);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_accum_list<32>, tpb, 0);
-    return (uint64_t)sms * (uint64_t)std::max(1, std::min(b0, b1)) * (uint64_t)tpb;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w0, k_accum_level0_wide<32>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w1, k_accum_list_wide<32>, tpb, 0);
+    Resident r;
+    r.narrow = (uint64_t)sms * (uint64_t)std::max(1, std::min(b0, b1)) * (uint64_t)tpb;
+    r.wide = (uint64_t)sms * (uint64_t)std::max(1, std::min(w0, w1)) * (uint64_t)tpb;
+    return r;
 }
 
 }  // namespace msm

@@ -355,7 +355,7 @@ struct msm_g1_ctx {
     uint32_t* phi;         // phi(P_i) = (beta x_i, y_i) for the GLV split
     int glv;               // 1: split scalars by the endomorphism (default)
     int finish_t;          // 0: automatic
-    uint64_t resident[3];  // resident accumulation threads for tpb = 64, 128, 256
+    Resident resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     int groups;            // window groups of the pipelined schedule (1 = serial)
     bool streams_ok;       // the context's own streams and events exist
     cudaStream_t acc_stream[MAX_GROUPS], chain_stream;
@@ -720,7 +720,7 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1;
     uint64_t pairs_total = 0;
     PairLayout lay = make_layout(terms, W, B, pipelined ? groups : 1, &pairs_total);
-    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, c->resident[1]));
+    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, c->resident[1].narrow));
     if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
@@ -733,7 +733,11 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     }
     mark(3);
     // the groups share the GPU in the pipelined schedule: size each grid for a share of it
-    const uint64_t resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2] / (pipelined ? 2 : 1);
+    Resident resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2];
+    if (pipelined) {
+        resident.narrow /= 2;
+        resident.wide /= 2;
+    }
     const uint32_t L = reduce_chunk_len(B);
     const uint32_t G = (B + L - 1) / L;
     // one window group: level 0, the tree levels, the bucket reduction
@@ -889,7 +893,7 @@ namespace {
 constexpr int kNoallocDevices = 64;
 std::mutex g_noalloc_lock;
 void* g_noalloc_ptr[kNoallocDevices];
-uint64_t g_noalloc_resident[kNoallocDevices][3];
+Resident g_noalloc_resident[kNoallocDevices][3];
 }  // namespace
 
 extern "C" int msm_g1_run_noalloc(const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
