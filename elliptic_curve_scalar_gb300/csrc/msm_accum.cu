@@ -87,7 +87,7 @@ struct Level0Src {
         uint32_t *__restrict__ items, ctl_t *ctl, int stats
 #define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats
 
-template <int S>
+template <int S, bool WIDE>
 __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     // units of buckets [g0, g1): pairs (2u, 2u+1) for u in [offset_g0 / 2, offset_g1 / 2)
     const uint32_t ubeg = offsets[g0] >> 1;
@@ -109,17 +109,17 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
         src.e0[k] = e.x;
         src.e1[k] = e.y;
     }
-    int adds = batch_pairs<S>(src, count);
+    int adds = batch_pairs<S, WIDE>(src, count);
     if (stats) warp_stats(ctl, adds, 1);
 }
 
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_level0(LEVEL0_PARAMS) {
-    accum_level0<S>(LEVEL0_ARGS);
+    accum_level0<S, false>(LEVEL0_ARGS);
 }
 template <int S>
 __global__ void __maxnreg__(80) k_accum_level0_wide(LEVEL0_PARAMS) {
-    accum_level0<S>(LEVEL0_ARGS);
+    accum_level0<S, true>(LEVEL0_ARGS);
 }
 
 // ------------------------------------------------------- pair lists per level
@@ -214,7 +214,7 @@ struct ListSrc {
     __device__ __forceinline__ void store(int k, const aff& r) { g1::store_aff(items + (size_t)qi[k] * 16, r); }
 };
 
-template <int S>
+template <int S, bool WIDE>
 __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
                                            ctl_t* ctl, int grp, int level, int stats) {
     const uint32_t cnt = ctl->pair_count[grp][level];
@@ -228,7 +228,7 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     src.items = items;
     src.half = 1u << (level - 1);
     for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
-    int adds = batch_pairs<S>(src, count);
+    int adds = batch_pairs<S, WIDE>(src, count);
     if (stats) {
         warp_stats(ctl, adds, 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
@@ -238,12 +238,12 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
                                                     ctl_t* ctl, int grp, int level, int stats) {
-    accum_list<S>(items, list, ctl, grp, level, stats);
+    accum_list<S, false>(items, list, ctl, grp, level, stats);
 }
 template <int S>
 __global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
                                                   ctl_t* ctl, int grp, int level, int stats) {
-    accum_list<S>(items, list, ctl, grp, level, stats);
+    accum_list<S, true>(items, list, ctl, grp, level, stats);
 }
 
 // ------------------------------------------------------------ small buckets

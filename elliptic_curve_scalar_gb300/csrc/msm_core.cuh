@@ -196,12 +196,20 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
 //   bool has_q(k); fe xp(k), xq(k); void ys(k, fe& yp, fe& yq);
 //   aff p(k), q(k); void store(k, const aff&).
 // Returns the number of slots that were true additions (ADD or DBL).
-template <int S, class Src>
+//
+// The per-slot loops stay rolled: unrolled, S copies of the inlined
+// multiplications overflow the instruction cache (the kernel then stalls on
+// instruction fetch) and pin S x 8 registers of prefix products.  The prefix
+// products live in thread-local memory.  The multiplications of Montgomery's
+// trick are inlined -- the forward one always, the two backward ones when
+// INLINE_BACK -- the others are called: inlined, a multiplication needs no
+// moves into and out of the call's argument registers (which occupy the same
+// multiply pipe the products do) and leaves the register allocator a global
+// view.  Inlining the backward pair pays for large, throughput-bound launches
+// (n = 2^22: 12.98 -> 12.79 ms) and costs latency-bound ones (n = 2^16: 1.27
+// -> 1.30 ms) through the larger loop body; inlining all six was slower still.
+template <int S, bool INLINE_BACK, class Src>
 __device__ __forceinline__ int batch_pairs(Src& src, int count) {
-    // The per-slot loops stay rolled: unrolled, S copies of the inlined
-    // multiplications overflow the instruction cache (the kernel then stalls
-    // on instruction fetch) and pin S x 8 registers of prefix products.  The
-    // prefix products live in thread-local memory, which stays in L1.
     fe pre[S];
     fe acc = fq::one();
     int adds = 0;
@@ -214,7 +222,7 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count) {
         int cs = pair_case(hq, xp, xq, [&](fe& a, fe& b) { src.ys(k, a, b); }, yp);
         fe d = pair_denominator(cs, xp, xq, yp);
         adds += (cs == PC_ADD || cs == PC_DBL);
-        acc = (k == 0) ? d : fq::mul(acc, d);
+        acc = (k == 0) ? d : fq::mul_inline(acc, d);
         pre[k] = acc;
     }
     fe inv = inv::inv_safegcd(acc);
@@ -228,8 +236,13 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count) {
         fe d = pair_denominator(cs, p.x, q.x, p.y);
         fe dinv = inv;
         if (k > 0) {
-            dinv = fq::mul(inv, pre[k - 1]);
-            inv = fq::mul(inv, d);
+            if (INLINE_BACK) {
+                dinv = fq::mul_inline(inv, pre[k - 1]);
+                inv = fq::mul_inline(inv, d);
+            } else {
+                dinv = fq::mul(inv, pre[k - 1]);
+                inv = fq::mul(inv, d);
+            }
         }
         src.store(k, pair_result(cs, p, q, dinv));
     }

@@ -62,7 +62,7 @@ _SIGS = {
     "msm_g1_strerror": (ctypes.c_char_p, [_i]),
     "msm_g1_test_fq": (_i, [_i, _vp, _vp, _vp, _sz, _vp]),
     "msm_g1_test_g1": (_i, [_i, _vp, _vp, _vp, _sz, _vp]),
-    "msm_g1_test_batch_add": (_i, [_vp, _vp, _vp, _sz, _i, _vp]),
+    "msm_g1_test_batch_add": (_i, [_vp, _vp, _vp, _sz, _i, _i, _vp]),
     "msm_g1_test_digits": (_i, [_vp, _sz, _i, _i, _vp, _vp]),
     "msm_g1_test_glv_split": (_i, [_vp, _sz, _vp, _vp]),
     "msm_g1_glv_constants": (_i, [_vp, _vp]),
@@ -269,11 +269,12 @@ def test_g1(op, a, b=None, stream=None):
     return out
 
 
-def test_batch_add(a, b, batch_s, stream=None):
+def test_batch_add(a, b, batch_s, inline_back=0, stream=None):
     n = a.shape[0]
     out = torch.empty_like(a)
     _check(lib().msm_g1_test_batch_add(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
-                                       ctypes.c_void_p(out.data_ptr()), n, batch_s, _stream_handle(stream)),
+                                       ctypes.c_void_p(out.data_ptr()), n, batch_s, inline_back,
+                                       _stream_handle(stream)),
            "msm_g1_test_batch_add")
     return out
 
