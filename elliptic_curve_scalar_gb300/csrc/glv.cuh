@@ -13,8 +13,9 @@
 // The split takes the short lattice basis v1 = (a1, b1), v2 = (a2, b2) of
 // {(x, y) : x + lambda y = 0 mod r}, found by the extended Euclidean
 // algorithm on (r, lambda) as the GLV paper does (a1 b2 - a2 b1 = r), and
-// rounds (k, 0) = x1 v1 + x2 v2 with x1 = k b2 / r, x2 = -k b1 / r to integers c_i = floor(k g_i / 2^256), where
-// g1 = round(b2 2^256 / r) and g2 = round(-b1 2^256 / r).  The rounding error
+// rounds (k, 0) = x1 v1 + x2 v2 with x1 = k b2 / r, x2 = -k b1 / r to the
+// integers c_i = floor(k g_i / 2^256), where g1 = round(b2 2^256 / r) and
+// g2 = round(-b1 2^256 / r).  The rounding error
 // |x_i - c_i| stays below 1 + 2^-3 for k < r, so
 //   k1 = k - c1 a1 - c2 a2,   k2 = -c1 b1 - c2 b2
 // satisfy |k_i| < 1.125 (a1 + a2) < 2^127 (a1 + a2 = |b1| + b2 ~ 2^126.8).

@@ -116,24 +116,28 @@ __device__ __forceinline__ void scalar_digits(const uint32_t* __restrict__ scala
 }
 
 // One thread per scalar; the lanes of a warp hitting the same bucket share one
-// atomic.  With GLV the kernel also writes phi(P_i) = (beta x_i, y_i).
+// atomic.
 template <bool GLV>
 __global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L,
-                              uint32_t* __restrict__ counts, const uint32_t* __restrict__ points,
-                              uint32_t* __restrict__ phi) {
+                              uint32_t* __restrict__ counts) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const bool live = i < n;
-    if (GLV && live) {
-        const fe beta = {{GLV_BETA_MONT}};
-        aff p = g1::load_aff(points + 16 * i);
-        p.x = fq::mul(p.x, beta);  // the point at infinity (0, 0) stays (0, 0)
-        g1::store_aff(phi + 16 * i, p);
-    }
     const int lane = threadIdx.x & 31;
     scalar_digits<GLV>(scalars, n, i, live, c, L, [&](uint32_t g, uint32_t) {
         const uint32_t peers = __match_any_sync(0xffffffffu, g);
         if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
     });
+}
+
+// GLV images phi(P_i) = (beta x_i, y_i); one thread per point.  Needs only the
+// points, so it runs beside the sort (which needs only the scalars).
+__global__ void k_phi(const uint32_t* __restrict__ points, size_t n, uint32_t* __restrict__ phi) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const fe beta = {{GLV_BETA_MONT}};
+    aff p = g1::load_aff(points + 16 * i);
+    p.x = fq::mul(p.x, beta);  // the point at infinity (0, 0) stays (0, 0)
+    g1::store_aff(phi + 16 * i, p);
 }
 
 // ---------------------------------------------------------------- 2. scan
@@ -360,6 +364,10 @@ struct msm_g1_ctx {
     bool streams_ok;       // the context's own streams and events exist
     cudaStream_t acc_stream[MAX_GROUPS], chain_stream;
     cudaEvent_t ev_fork, ev_group[MAX_GROUPS], ev_chain;
+    cudaStream_t side_stream;    // points upload and phi beside the sort
+    cudaEvent_t ev_side, ev_points;
+    uint32_t* stage;             // host-buffer entry: device copies of points, scalars and the result
+    size_t stage_n;
     ctl_t* ctl;
     bool gen_ready;
     int batch_s, tpb, timing, stats;
@@ -586,6 +594,9 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
         for (int j = 0; j < MAX_GROUPS; j++)
             ok = ok && cudaStreamCreateWithPriority(&c->acc_stream[j], cudaStreamNonBlocking, lo) == cudaSuccess;
         ok = ok && cudaStreamCreateWithPriority(&c->chain_stream, cudaStreamNonBlocking, hi) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&c->side_stream, cudaStreamNonBlocking, hi) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&c->ev_side, cudaEventDisableTiming) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&c->ev_points, cudaEventDisableTiming) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
         ok = ok && cudaEventCreateWithFlags(&c->ev_chain, cudaEventDisableTiming) == cudaSuccess;
         for (int j = 0; j < MAX_GROUPS; j++)
@@ -605,6 +616,10 @@ void msm_g1_destroy(msm_g1_ctx* c) {
     for (int j = 0; j < MAX_GROUPS; j++)
         if (c->acc_stream[j]) cudaStreamDestroy(c->acc_stream[j]);
     if (c->chain_stream) cudaStreamDestroy(c->chain_stream);
+    if (c->side_stream) cudaStreamDestroy(c->side_stream);
+    if (c->ev_side) cudaEventDestroy(c->ev_side);
+    if (c->ev_points) cudaEventDestroy(c->ev_points);
+    if (c->stage) cudaFree(c->stage);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_chain) cudaEventDestroy(c->ev_chain);
     for (int j = 0; j < MAX_GROUPS; j++)
@@ -666,10 +681,10 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
 
 }  // extern "C"
 
-extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
-                          uint32_t* out, cudaStream_t st) {
-    if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
-    if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
+// The MSM.  points_host: when non-null, the points are copied from this host
+// buffer into `points` (device) on the side stream while the sort runs.
+static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
+                    uint32_t* out, cudaStream_t st, const uint32_t* points_host) {
     int cw = window_c == 0 ? std::min(msm_g1_auto_window(n), c->max_c) : window_c;
     if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
     if (cw > c->max_c || n > c->max_n) return MSM_G1_ERR_CAPACITY;
@@ -699,13 +714,34 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     }
     const int stats = c->stats;
     int launches = 0;
+    // Points side: upload (host-buffer entry) and phi need only the points and
+    // run on the side stream beside the sort, which needs only the scalars;
+    // level 0 waits for them.  With phase timing (or without context streams)
+    // they run in order on the calling stream, inside the first phase.
+    const bool side = c->streams_ok && !c->timing;
+    auto points_side = [&](cudaStream_t s) -> int {
+        if (points_host) CK(cudaMemcpyAsync((void*)points, points_host, 64ull * n, cudaMemcpyHostToDevice, s));
+        if (glv) {
+            k_phi<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(points, n, c->phi);
+            launches++;
+        }
+        return MSM_G1_OK;
+    };
     mark(0);
+    if (side) {
+        CK(cudaEventRecord(c->ev_side, st));
+        CK(cudaStreamWaitEvent(c->side_stream, c->ev_side, 0));
+        if (points_side(c->side_stream) != MSM_G1_OK) return MSM_G1_ERR_CUDA;
+        CK(cudaEventRecord(c->ev_points, c->side_stream));
+    } else if (points_side(st) != MSM_G1_OK) {
+        return MSM_G1_ERR_CUDA;
+    }
     CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
     CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
-        if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts, points, c->phi);
-        else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts, points, c->phi);
+        if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts);
+        else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts);
         launches++;
     }
     mark(1);
@@ -742,6 +778,7 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     const uint32_t G = (B + L - 1) / L;
     // one window group: level 0, the tree levels, the bucket reduction
     auto level0 = [&](int j, cudaStream_t s) {
+        if (side) cudaStreamWaitEvent(s, c->ev_points, 0);
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         launch_accum_level0(c->batch_s, c->tpb, resident, points, c->phi, nsplit, c->entries, c->offsets,
                             (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
@@ -806,6 +843,40 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     c->last_launches = launches;
     if (cudaGetLastError() != cudaSuccess) return MSM_G1_ERR_CUDA;
     c->have_timing = c->timing != 0;
+    return MSM_G1_OK;
+}
+
+extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
+                          uint32_t* out, cudaStream_t st) {
+    if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
+    if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
+    return run_core(c, points, scalars, n, window_c, out, st, nullptr);
+}
+
+extern "C" int msm_g1_run_host(msm_g1_ctx* c, const uint32_t* points_host, const uint32_t* scalars_host, size_t n,
+                               int window_c, uint32_t* out_host, cudaStream_t st) {
+    if (!c || !out_host) return MSM_G1_ERR_INVALID_ARG;
+    if (n > 0 && (!points_host || !scalars_host)) return MSM_G1_ERR_INVALID_ARG;
+    if (n > c->max_n) return MSM_G1_ERR_CAPACITY;
+    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
+    if (!c->stage) {  // first call: device copies of points, scalars and the result, for max_n
+        size_t bytes = 96 * c->max_n + 256;
+        if (cudaMalloc((void**)&c->stage, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            c->stage = nullptr;
+            return MSM_G1_ERR_ALLOC;
+        }
+        c->stage_n = c->max_n;
+    }
+    uint32_t* pts = c->stage;
+    uint32_t* sc = c->stage + 16 * c->stage_n;
+    uint32_t* res = c->stage + 24 * c->stage_n;  // 96 B, 16-byte aligned (offset 96 max_n)
+    if (n > 0) CK(cudaMemcpyAsync(sc, scalars_host, 32ull * n, cudaMemcpyHostToDevice, st));
+    // the points are copied by run_core beside the sort (in order on st when
+    // the context has no streams or times phases)
+    int rc = run_core(c, pts, sc, n, window_c, res, st, n > 0 ? points_host : nullptr);
+    if (rc != MSM_G1_OK) return rc;
+    CK(cudaMemcpyAsync(out_host, res, 96, cudaMemcpyDeviceToHost, st));
     return MSM_G1_OK;
 }
 

@@ -50,6 +50,7 @@ _SIGS = {
     "msm_g1_create": (_i, [ctypes.POINTER(_vp), _sz, _i]),
     "msm_g1_run": (_i, [_vp, _vp, _vp, _sz, _i, _vp, _vp]),
     "msm_g1_run_noalloc": (_i, [_vp, _vp, _sz, _i, _vp, _vp]),
+    "msm_g1_run_host": (_i, [_vp, _vp, _vp, _sz, _i, _vp, _vp]),
     "msm_g1_mul_generator": (_i, [_vp, _vp, _sz, _vp, _vp]),
     "msm_g1_destroy": (None, [_vp]),
     "msm_g1_set_param": (_i, [_vp, _i, _i]),
@@ -197,6 +198,25 @@ class MsmG1:
         op = ctypes.c_void_p(out.data_ptr())
         with torch.cuda.device(self.device):
             _check(lib().msm_g1_run(self._ctx, pp, sp, n, c, op, _stream_handle(stream)), "msm_g1_run")
+        return out
+
+    def run_host(self, points, scalars, c=0, out=None, stream=None):
+        """msm_g1_run_host: inputs and result in host memory (CPU torch tensors,
+        pinned for asynchronous copies).  Returns the (24,) int32 CPU result
+        tensor, valid once the stream has been synchronised."""
+        n = scalars.shape[0]
+        if points.shape[0] != n:
+            raise ValueError("points and scalars differ in length")
+        for t, tail, what in ((points, (16,), "points"), (scalars, (8,), "scalars")):
+            if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous() \
+                    or tuple(t.shape[1:]) != tail:
+                raise TypeError("%s must be a contiguous CPU torch.int32 tensor of shape (n,) + %s" % (what, tail))
+        if out is None:
+            out = torch.empty(24, dtype=torch.int32).pin_memory()
+        with torch.cuda.device(self.device):
+            _check(lib().msm_g1_run_host(self._ctx, ctypes.c_void_p(points.data_ptr()),
+                                         ctypes.c_void_p(scalars.data_ptr()), n, c, ctypes.c_void_p(out.data_ptr()),
+                                         _stream_handle(stream)), "msm_g1_run_host")
         return out
 
     def mul_generator(self, scalars, out=None, stream=None):

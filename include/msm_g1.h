@@ -95,6 +95,20 @@ int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
 int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
                int window_c, uint32_t *out_jacobian, cudaStream_t stream);
 
+/* The same MSM with inputs and output in HOST memory: points_affine (n x 16
+ * uint32), scalars (n x 8 uint32) and out_jacobian (24 uint32), layouts as for
+ * msm_g1_run.  The call queues, on `stream`, the upload of the scalars, the
+ * MSM and the download of the result; the points are uploaded on one of the
+ * context's own streams while the sort (which needs only the scalars) runs,
+ * and the accumulation waits for them.  The first call allocates device
+ * copies for max_n points and scalars (synchronous; MSM_G1_ERR_ALLOC on
+ * failure).  With pinned (page-locked) host buffers every copy is
+ * asynchronous and the caller reads out_jacobian after synchronising
+ * `stream`; with pageable buffers CUDA stages the copies and may block.  The
+ * host buffers must stay valid until the stream reaches the end of the call. */
+int msm_g1_run_host(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
+                    int window_c, uint32_t *out_jacobian, cudaStream_t stream);
+
 /* out_i = [k_i]G for the generator G = (1, 2), as affine Montgomery points
  * (n x 16 uint32, infinity as (0, 0)).  scalars: device, n x 8 uint32, any
  * 256-bit value.  A utility for building workloads P_i = [r_i]G on the device;

@@ -83,6 +83,7 @@ def test_argument_checks_before_device_work(lib):
     assert lib.msm_g1_create(ctypes.byref(ctx), 16, 21) == gm.ERR_INVALID_ARG
     assert not ctx.value
     assert lib.msm_g1_run(None, None, None, 0, 8, None, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_run_host(None, None, None, 0, 8, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_set_param(None, gm.PARAM_BATCH_S, 8) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_mul_generator(None, None, 0, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_test_fq(99, None, None, None, 1, None) == gm.ERR_INVALID_ARG

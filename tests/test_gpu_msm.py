@@ -122,6 +122,66 @@ def test_small_bucket_finish(mid_case, finish_t):
     assert np.array_equal(got, expect)
 
 
+def _host_inputs(pts, k, pin=True):
+    p = torch.from_numpy(oracle.points_to_gpu_layout(pts).view(np.int32))
+    s_ = torch.from_numpy(synth.scalars_to_u32(k).view(np.int32))
+    return (p.pin_memory(), s_.pin_memory()) if pin else (p.contiguous(), s_.contiguous())
+
+
+@pytest.mark.parametrize("glv", [1, 0])
+@pytest.mark.parametrize("timing", [0, 1])
+def test_host_buffer_entry(mid_case, glv, timing):
+    """msm_g1_run_host (inputs and result in host memory, the points uploaded
+    on a context stream beside the sort) gives the oracle's result in both
+    schedules."""
+    pts, k, expect = mid_case
+    cx = ctx(20000, 13)
+    cx.set_param(gm.PARAM_GLV, glv)
+    cx.set_param(gm.PARAM_TIMING, timing)
+    try:
+        hp, hs = _host_inputs(pts, k)
+        out = cx.run_host(hp, hs, 13)
+        got = normalise(out)
+    finally:
+        cx.set_param(gm.PARAM_GLV, 1)
+        cx.set_param(gm.PARAM_TIMING, 0)
+    assert np.array_equal(got, expect)
+
+
+def test_host_buffer_entry_back_to_back():
+    """Consecutive host-buffer calls on one stream with no synchronisation in
+    between reuse the context's device copies: each must still see its own
+    inputs (pinned and pageable host buffers)."""
+    cases = []
+    for i, n in enumerate((3000, 1500, 2999)):
+        r, k = synth.uniform_workload(n, 7100 + i)
+        pts = points_from_r(r)
+        cases.append((pts, k, oracle.closed_form(r, k), i != 1))
+    cx = ctx(3000, 11)
+    outs = []
+    for pts, k, _, pin in cases:
+        hp, hs = _host_inputs(pts, k, pin)
+        outs.append(cx.run_host(hp, hs, 11, out=torch.empty(24, dtype=torch.int32).pin_memory()))
+    torch.cuda.synchronize()
+    for (pts, k, expect, _), out in zip(cases, outs):
+        assert np.array_equal(normalise(out), expect)
+
+
+def test_host_buffer_entry_edges():
+    cx = ctx(100, 8)
+    empty_p = torch.zeros((0, 16), dtype=torch.int32)
+    empty_s = torch.zeros((0, 8), dtype=torch.int32)
+    out = cx.run_host(empty_p, empty_s, 8)
+    assert oracle.words_to_point(normalise(out)) is None
+    r, k = synth.uniform_workload(101, 3)
+    hp, hs = _host_inputs(points_from_r(r), k)
+    with pytest.raises(gm.MsmError) as e:
+        cx.run_host(hp, hs, 8)
+    assert e.value.code == gm.ERR_CAPACITY
+    out = cx.run_host(hp[:100], hs[:100], 8)
+    assert np.array_equal(normalise(out), oracle.closed_form(r[:100], k[:100]))
+
+
 def test_empty_input():
     cx = ctx(16, 8)
     pts = torch.zeros((0, 16), dtype=torch.int32, device="cuda")
