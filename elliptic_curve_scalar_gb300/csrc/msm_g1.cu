@@ -47,6 +47,8 @@ constexpr int SCAN_TPB = 256;
 constexpr int SCAN_ITEMS = 8;
 constexpr int SCAN_TILE = SCAN_TPB * SCAN_ITEMS;
 constexpr int REDUCE_TPB = 256;
+constexpr uint32_t MAX_REDUCE_JOBS = 16;  // 1 + log2 G, G <= 2^12 (one warp per job)
+constexpr uint32_t REDUCE_MAX_PARTS = 8;  // partial blocks per reduction job
 
 // ---------------------------------------------------------------- helpers
 
@@ -233,9 +235,18 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
 }
 
 // ---------------------------------------------------------- 6. reduction
+//
+// T_w = sum_{b<B} (b + 1) S_b per window, without a per-chunk scalar multiple.
+// Buckets are cut into G = B / L chunks of L; chunk j yields its plain sum
+// R_j and its local weighted sum C_j = sum_{i<L} (i + 1) S_{jL+i}, so that
+//     T_w = sum_j C_j + L sum_j j R_j,   sum_j j R_j = sum_t 2^t V_t,
+// V_t = sum of the R_j whose index j has bit t set.  The 1 + log2 G plain sums
+// (sum C_j and every V_t) are wide tree reductions; only a log2 G-step Horner
+// pass (one doubling and one addition per bit) and log2 L doublings remain
+// sequential, run by one warp with the warp-cooperative point operations.
 
-// One thread per chunk of L consecutive buckets of one window:
-// C_j = sum_{i<L} (jL + i + 1) S_{jL+i} via running sums from the top bucket.
+// One thread per chunk: running sums from the chunk's top bucket give
+// run = R_j and sum = C_j (bucket jL + i is added into run at steps i .. 0).
 __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ counts,
                                 const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ jsum,
                                 uint32_t finish_t, int w_lo, int nwin, uint32_t B, uint32_t L, uint32_t G,
@@ -257,29 +268,98 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
         }
         sum = g1::add(sum, run);
     }
-    if (b0) sum = g1::add(sum, g1::mul_small(run, b0));
-    g1::store_jac(chunks + ((size_t)w * G + j) * 24, sum);
+    uint32_t* dst = chunks + ((size_t)w * G + j) * 48;
+    g1::store_jac(dst, sum);
+    g1::store_jac(dst + 24, run);
 }
 
-// One block per window: T_w = sum_j C_j (strided partial sums, then a tree).
-__global__ void __launch_bounds__(REDUCE_TPB) k_reduce_windows(const uint32_t* __restrict__ chunks, int w_lo,
-                                                               uint32_t G, uint32_t* __restrict__ wsums) {
-    __shared__ uint32_t sm[REDUCE_TPB * 24];
-    uint32_t w = (uint32_t)w_lo + blockIdx.x;
-    jac acc = g1::jac_inf();
-    for (uint32_t j = threadIdx.x; j < G; j += blockDim.x)
-        acc = g1::add(acc, g1::load_jac(chunks + ((size_t)w * G + j) * 24));
-    g1::store_jac(sm + threadIdx.x * 24, acc);
-    __syncthreads();
-    for (uint32_t s = blockDim.x / 2; s > 0; s >>= 1) {
-        if (threadIdx.x < s) {
-            jac o = g1::load_jac(sm + (threadIdx.x + s) * 24);
-            acc = g1::add(acc, o);
-            g1::store_jac(sm + threadIdx.x * 24, acc);
+// Sum of the n Jacobian points in sm[0 .. n) (n a power of two, n <= blockDim.x
+// <= 256, one point per thread slot); the result lands in sm[0].  Wide levels
+// use one thread per addition; the last five (32 points down to 1) use a whole
+// warp per addition, whose latency is a third of one thread's.
+__device__ void block_tree_sum(uint32_t* sm, uint32_t n) {
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    uint32_t s = n;
+    for (; s > 32; s >>= 1) {
+        const uint32_t h = s >> 1;
+        if (tid < h) g1::store_jac(sm + tid * 24, g1::add(g1::load_jac(sm + tid * 24), g1::load_jac(sm + (tid + h) * 24)));
+        __syncthreads();
+    }
+    for (; s > 1; s >>= 1) {
+        const uint32_t h = s >> 1;
+        for (uint32_t q = warp; q < h; q += nwarps) {
+            jac r = g1c::add(g1::load_jac(sm + q * 24), g1::load_jac(sm + (q + h) * 24));
+            __syncwarp();
+            if ((tid & 31) == 0) g1::store_jac(sm + q * 24, r);
         }
         __syncthreads();
     }
-    if (threadIdx.x == 0) g1::store_jac(wsums + (size_t)w * 24, acc);
+}
+
+// Job 0 of a window sums every C_j; job 1 + t sums the R_j with bit t of j set.
+// Block (w, job, part) sums the job's terms [part 256 m, (part + 1) 256 m), m per thread.
+__global__ void __launch_bounds__(REDUCE_TPB) k_reduce_jobs(const uint32_t* __restrict__ chunks, int w_lo, uint32_t G,
+                                                            uint32_t jobs, uint32_t parts, uint32_t m,
+                                                            uint32_t* __restrict__ partials) {
+    __shared__ uint32_t sm[REDUCE_TPB * 24];
+    const uint32_t part = blockIdx.x % parts, job = (blockIdx.x / parts) % jobs;
+    const uint32_t w = (uint32_t)w_lo + blockIdx.x / (parts * jobs);
+    const uint32_t terms = job == 0 ? G : G >> 1;
+    const uint32_t tb = job == 0 ? 0 : job - 1;  // the bit of job 1 + tb
+    jac acc = g1::jac_inf();
+    const uint32_t k0 = (part * blockDim.x + threadIdx.x) * m;
+    for (uint32_t k = k0; k < k0 + m && k < terms; k++) {
+        uint32_t jdx, half;
+        if (job == 0) {
+            jdx = k;
+            half = 0;  // C_j
+        } else {  // the k-th index with bit tb set
+            jdx = ((k >> tb) << (tb + 1)) | (1u << tb) | (k & ((1u << tb) - 1u));
+            half = 24;  // R_j
+        }
+        acc = g1::add(acc, g1::load_jac(chunks + ((size_t)w * G + jdx) * 48 + half));
+    }
+    g1::store_jac(sm + threadIdx.x * 24, acc);
+    __syncthreads();
+    block_tree_sum(sm, blockDim.x);
+    if (threadIdx.x < 24) partials[((size_t)(w * jobs + job) * parts + part) * 24 + threadIdx.x] = sm[threadIdx.x];
+}
+
+// One block per window, one warp per job: warp q sums its job's partial sums
+// and shifts the result to its weight -- V_t by 2^t L (t + log2 L doublings),
+// the sum of C_j not at all -- so that the bits are weighted in parallel
+// rather than by a sequential Horner pass; a tree over the jobs' values then
+// gives T_w = sum C_j + L sum_t 2^t V_t.
+__global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uint32_t* __restrict__ partials, int w_lo,
+                                                                       uint32_t jobs, uint32_t parts, uint32_t log2L,
+                                                                       uint32_t* __restrict__ wsums) {
+    __shared__ uint32_t sm[MAX_REDUCE_JOBS * 24];
+    const uint32_t w = (uint32_t)w_lo + blockIdx.x;
+    const uint32_t q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t span = 1;
+    while (span < jobs) span <<= 1;
+    // the tree runs over span = 2^k >= jobs values; the block has one warp per
+    // job, so its first threads set the span - jobs padding values to infinity
+    if (threadIdx.x < span - jobs) g1::store_jac(sm + (jobs + threadIdx.x) * 24, g1::jac_inf());
+    if (q < jobs) {
+        const uint32_t* src = partials + (size_t)(w * jobs + q) * parts * 24;
+        jac acc = g1::load_jac(src);
+        for (uint32_t p = 1; p < parts; p++) acc = g1c::add(acc, g1::load_jac(src + p * 24));
+        const uint32_t shift = q == 0 ? 0 : q - 1 + log2L;
+        for (uint32_t i = 0; i < shift; i++) acc = g1c::dbl(acc);
+        __syncwarp();
+        if (lane == 0) g1::store_jac(sm + q * 24, acc);
+    }
+    __syncthreads();
+    for (uint32_t h = span >> 1; h >= 1; h >>= 1) {
+        if (q < h) {
+            jac r = g1c::add(g1::load_jac(sm + q * 24), g1::load_jac(sm + (q + h) * 24));
+            __syncwarp();
+            if (lane == 0) g1::store_jac(sm + q * 24, r);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x < 24) wsums[(size_t)w * 24 + threadIdx.x] = sm[threadIdx.x];
 }
 
 // ---------------------------------------------------------- 7. combination
@@ -353,6 +433,7 @@ struct msm_g1_ctx {
     size_t scratch_bytes;
     char* scratch;
     uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
+    uint32_t* partials;    // partial sums of the bucket-reduction jobs
     uint32_t* pairs;
     uint32_t* qacc;        // running value of the window combination between groups
     uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
@@ -381,15 +462,43 @@ struct msm_g1_ctx {
 static int window_count(int c) { return make_windows(c, PLAIN_BITS).W; }
 static int glv_window_count(int c) { return make_windows(c, GLV_BITS).W; }
 static uint32_t reduce_chunk_len(uint32_t B) {
-    // L ~ sqrt(B / 512), a power of two, at least 4: balances the per-thread
-    // running-sum chain against the per-window tree
+    // L = 4 keeps each chunk's running sum short (2L additions); from B = 2^13
+    // on, L grows so that G = B / L stays <= 2^12 and the subset sums of the
+    // reduction ((1 + log2 G) G / 2 additions per window) stay small
+    // (measured at n = 2^22, c = 16: G = 8192 made the subset sums 0.36 ms)
     uint32_t L = 4;
-    while ((uint64_t)L * L * 512 < B) L <<= 1;
+    while ((uint64_t)L * 4096 < B) L <<= 1;
     return std::min(L, B);
 }
 
+static uint32_t ilog2(uint32_t x) {
+    uint32_t r = 0;
+    while ((1u << (r + 1)) <= x) r++;
+    return r;
+}
+
+// Reduction jobs of one window (sum of C_j, and one V_t per bit of the chunk
+// index) and their split into partial blocks of 256 threads x m terms.
+struct ReducePlan {
+    uint32_t L, G, jobs, parts, m;
+};
+// m, the terms each thread adds before the block tree, is the smallest power
+// of two that keeps parts <= REDUCE_MAX_PARTS (a longer per-thread chain cost
+// more than a second wave of blocks when measured).
+static ReducePlan reduce_plan(uint32_t B) {
+    ReducePlan r;
+    r.L = reduce_chunk_len(B);
+    r.G = B / r.L;
+    r.jobs = 1 + ilog2(r.G);
+    r.m = 1;
+    auto parts_for = [&](uint32_t m) { return (r.G + 256 * m - 1) / (256 * m); };
+    while (parts_for(r.m) > REDUCE_MAX_PARTS) r.m <<= 1;
+    r.parts = parts_for(r.m);
+    return r;
+}
+
 struct sizing {
-    uint64_t points, entries, buckets, chunks, pairs;
+    uint64_t points, entries, buckets, chunks, pairs, partials;
 };
 
 // Level pair-list capacities for at most h_ub level-1 items in nb buckets:
@@ -438,7 +547,7 @@ static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_
 }
 
 static sizing size_for(size_t max_n, int max_c) {
-    sizing s{max_n, 0, 0, 0, 0};
+    sizing s{max_n, 0, 0, 0, 0, 0};
     // entries for windows down to 8 bits (smaller windows fit smaller n); the
     // GLV split doubles the terms and about halves the windows
     const int cmin = std::min(max_c, 8);
@@ -446,9 +555,11 @@ static sizing size_for(size_t max_n, int max_c) {
     for (int c = 1; c <= max_c; c++) {
         uint64_t B = 1ull << (c - 1);
         uint64_t wb = (uint64_t)window_count(c) * B;
-        uint64_t wg = (uint64_t)window_count(c) * ((B + reduce_chunk_len((uint32_t)B) - 1) / reduce_chunk_len((uint32_t)B));
+        const ReducePlan rp = reduce_plan((uint32_t)B);
+        const uint64_t wg = (uint64_t)window_count(c) * rp.G;
         s.buckets = std::max(s.buckets, wb);
         s.chunks = std::max(s.chunks, wg);
+        s.partials = std::max(s.partials, (uint64_t)window_count(c) * rp.jobs * rp.parts);
     }
     s.entries += s.buckets;  // one padding entry per bucket at most
     s.entries += 2;
@@ -483,7 +594,8 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_tiles = take(4 * (s.buckets / SCAN_TILE + 2));
     size_t o_entries = take(4 * s.entries);
     size_t o_items = take((size_t)64 * ((s.entries + 1) / 2));
-    size_t o_chunks = take((size_t)96 * s.chunks);
+    size_t o_chunks = take((size_t)192 * s.chunks);  // C_j, R_j per chunk
+    size_t o_partials = take((size_t)96 * s.partials);
     size_t o_wsums = take((size_t)96 * 256);
     size_t o_table = take((size_t)64 * 256);
     size_t o_tj = take((size_t)96 * 256);
@@ -504,6 +616,7 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
         c->entries = (uint32_t*)(c->scratch + o_entries);
         c->items = (uint32_t*)(c->scratch + o_items);
         c->chunks = (uint32_t*)(c->scratch + o_chunks);
+        c->partials = (uint32_t*)(c->scratch + o_partials);
         c->wsums = (uint32_t*)(c->scratch + o_wsums);
         c->gen_table = (uint32_t*)(c->scratch + o_table);
         c->gen_tj = (uint32_t*)(c->scratch + o_tj);
@@ -774,8 +887,9 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         resident.narrow /= 2;
         resident.wide /= 2;
     }
-    const uint32_t L = reduce_chunk_len(B);
-    const uint32_t G = (B + L - 1) / L;
+    const ReducePlan rp = reduce_plan(B);
+    const uint32_t L = rp.L, G = rp.G;
+    if (rp.jobs > MAX_REDUCE_JOBS) return MSM_G1_ERR_INVALID_ARG;  // unreachable for c <= 20
     // one window group: level 0, the tree levels, the bucket reduction
     auto level0 = [&](int j, cudaStream_t s) {
         if (side) cudaStreamWaitEvent(s, c->ev_points, 0);
@@ -802,8 +916,10 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         }
         k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum, lay.finish_t,
                                                              lay.w_lo[j], nw, B, L, G, c->chunks);
-        k_reduce_windows<<<nw, REDUCE_TPB, 0, s>>>(c->chunks, lay.w_lo[j], G, c->wsums);
-        launches += 2;
+        k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, REDUCE_TPB, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
+                                                                              rp.parts, rp.m, c->partials);
+        k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L), c->wsums);
+        launches += 3;
     };
     auto combine = [&](int j, cudaStream_t s) {
         k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
