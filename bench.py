@@ -35,6 +35,9 @@ CONFIGS = {
     "n2p20": dict(n=1 << 20, c=16, kind="uniform", seed=1003),
     "n2p22": dict(n=1 << 22, c=16, kind="uniform", seed=1004),
     "n2p20adv": dict(n=1 << 20, c=16, kind="adversarial", seed=1006),
+    # larger than the pages' sizes (not bench defaults)
+    "n2p23": dict(n=1 << 23, c=16, kind="uniform", seed=1007),
+    "n2p24": dict(n=1 << 24, c=16, kind="uniform", seed=1008),
 }
 
 # Pages' own figure for this metric and workload: Apple M2 (WebGPU, Chrome 148),
@@ -69,6 +72,7 @@ def parse():
     ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
     ap.add_argument("--glv", type=int, default=1, choices=[0, 1], help="split scalars by the GLV endomorphism")
+    ap.add_argument("--inversion", type=int, default=0, choices=[0, 1], help="0: safegcd, 1: Fermat")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -193,6 +197,7 @@ def run_gpu(args, cfg):
     ctx.set_param(gm.PARAM_FINISH, args.finish)
     ctx.set_param(gm.PARAM_GROUPS, args.groups)
     ctx.set_param(gm.PARAM_GLV, args.glv)
+    ctx.set_param(gm.PARAM_INVERSION, args.inversion)
     scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
     # points P_i = [r_i]G built on the device by the library's fixed-base kernel
     pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
@@ -339,7 +344,8 @@ def run_gpu(args, cfg):
                          "count_basis": "6 Fq muls per addition x 264 IMAD slots per mul (128 full limb products at 2 slots + 8 low; inversion excluded)",
                          "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
-                         "inversion": "safegcd (Bernstein-Yang divsteps), one per %d additions" % args.batch_s,
+                         "inversion": "%s, one per %d additions" % (
+                             "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)", args.batch_s),
                          "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,

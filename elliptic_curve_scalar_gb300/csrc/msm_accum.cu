@@ -84,8 +84,8 @@ struct Level0Src {
 #define LEVEL0_PARAMS                                                                                     \
     const uint32_t *__restrict__ points, const uint32_t *__restrict__ phi, uint32_t nsplit,                \
         const uint32_t *__restrict__ entries, const uint32_t *__restrict__ offsets, uint32_t g0, uint32_t g1, \
-        uint32_t *__restrict__ items, ctl_t *ctl, int stats
-#define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats
+        uint32_t *__restrict__ items, ctl_t *ctl, int stats, int inv_kind
+#define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind
 
 template <int S, bool WIDE>
 __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
@@ -109,7 +109,7 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
         src.e0[k] = e.x;
         src.e1[k] = e.y;
     }
-    int adds = batch_pairs<S, WIDE>(src, count);
+    int adds = batch_pairs<S, WIDE>(src, count, inv_kind);
     if (stats) warp_stats(ctl, adds, 1);
 }
 
@@ -216,7 +216,7 @@ struct ListSrc {
 
 template <int S, bool WIDE>
 __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                           ctl_t* ctl, int grp, int level, int stats) {
+                                           ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
     const uint32_t cnt = ctl->pair_count[grp][level];
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
@@ -228,7 +228,7 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     src.items = items;
     src.half = 1u << (level - 1);
     for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
-    int adds = batch_pairs<S, WIDE>(src, count);
+    int adds = batch_pairs<S, WIDE>(src, count, inv_kind);
     if (stats) {
         warp_stats(ctl, adds, 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
@@ -237,13 +237,13 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
 
 template <int S>
 __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                    ctl_t* ctl, int grp, int level, int stats) {
-    accum_list<S, false>(items, list, ctl, grp, level, stats);
+                                                    ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
+    accum_list<S, false>(items, list, ctl, grp, level, stats, inv_kind);
 }
 template <int S>
 __global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                  ctl_t* ctl, int grp, int level, int stats) {
-    accum_list<S, true>(items, list, ctl, grp, level, stats);
+                                                  ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
+    accum_list<S, true>(items, list, ctl, grp, level, stats, inv_kind);
 }
 
 // ------------------------------------------------------------ small buckets
@@ -284,28 +284,31 @@ static bool wide(uint64_t work, int S, const Resident& res) { return (work + S -
 template <int S>
 static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
                      const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
-                     ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
+                     ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
     if (wide(units_ub, S, res))
-        k_accum_level0_wide<S><<<grid_for(units_ub, S, tpb, res.wide), tpb, 0, st>>>(points, phi, nsplit, entries,
-                                                                                    offsets, g0, g1, items, ctl, stats);
+        k_accum_level0_wide<S><<<grid_for(units_ub, S, tpb, res.wide), tpb, 0, st>>>(
+            points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
     else
-        k_accum_level0<S><<<grid_for(units_ub, S, tpb, res.narrow), tpb, 0, st>>>(points, phi, nsplit, entries,
-                                                                                 offsets, g0, g1, items, ctl, stats);
+        k_accum_level0<S><<<grid_for(units_ub, S, tpb, res.narrow), tpb, 0, st>>>(
+            points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
 }
 
 template <int S>
 static void list_t(int tpb, const Resident& res, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
-                   int grp, int level, int stats, cudaStream_t st) {
+                   int grp, int level, int stats, int inv_kind, cudaStream_t st) {
     if (wide(cap, S, res))
-        k_accum_list_wide<S><<<grid_for(cap, S, tpb, res.wide), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
+        k_accum_list_wide<S><<<grid_for(cap, S, tpb, res.wide), tpb, 0, st>>>(items, list, ctl, grp, level, stats,
+                                                                              inv_kind);
     else
-        k_accum_list<S><<<grid_for(cap, S, tpb, res.narrow), tpb, 0, st>>>(items, list, ctl, grp, level, stats);
+        k_accum_list<S><<<grid_for(cap, S, tpb, res.narrow), tpb, 0, st>>>(items, list, ctl, grp, level, stats,
+                                                                          inv_kind);
 }
 
 void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi,
                          uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st) {
-#define L0(S) level0_t<S>(tpb, res, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, st)
+                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
+#define L0(S) \
+    level0_t<S>(tpb, res, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, inv_kind, st)
     switch (batch_s) {
         case 1: L0(1); break;
         case 2: L0(2); break;
@@ -323,10 +326,11 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
 }
 
 void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st) {
+                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                        cudaStream_t st) {
     const uint32_t* list = pairs + lay.base[grp][level];
     uint64_t cap = lay.cap[grp][level];
-#define LV(S) list_t<S>(tpb, res, items, list, ctl, cap, grp, level, stats, st)
+#define LV(S) list_t<S>(tpb, res, items, list, ctl, cap, grp, level, stats, inv_kind, st)
     switch (batch_s) {
         case 1: LV(1); break;
         case 2: LV(2); break;

@@ -208,8 +208,10 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
 // view.  Inlining the backward pair pays for large, throughput-bound launches
 // (n = 2^22: 12.98 -> 12.79 ms) and costs latency-bound ones (n = 2^16: 1.27
 // -> 1.30 ms) through the larger loop body; inlining all six was slower still.
+// inv_kind selects the batch inversion: 0 = safegcd divsteps (the default),
+// 1 = Fermat (a^(p-2), 4-bit windows) -- kept for the measured comparison.
 template <int S, bool INLINE_BACK, class Src>
-__device__ __forceinline__ int batch_pairs(Src& src, int count) {
+__device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0) {
     fe pre[S];
     fe acc = fq::one();
     int adds = 0;
@@ -225,7 +227,7 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count) {
         acc = (k == 0) ? d : fq::mul_inline(acc, d);
         pre[k] = acc;
     }
-    fe inv = inv::inv_safegcd(acc);
+    fe inv = inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
 #pragma unroll 1
     for (int k = count - 1; k >= 0; k--) {
         aff p = src.p(k);

@@ -439,6 +439,7 @@ struct msm_g1_ctx {
     uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
     uint32_t* phi;         // phi(P_i) = (beta x_i, y_i) for the GLV split
     int glv;               // 1: split scalars by the endomorphism (default)
+    int inv_kind;          // batch inversion: 0 safegcd (default), 1 Fermat
     int finish_t;          // 0: automatic
     Resident resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     int groups;            // window groups of the pipelined schedule (1 = serial)
@@ -773,6 +774,10 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
             c->glv = value;
             return MSM_G1_OK;
+        case MSM_G1_PARAM_INVERSION:
+            if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
+            c->inv_kind = value;
+            return MSM_G1_OK;
         default:
             return MSM_G1_ERR_INVALID_ARG;
     }
@@ -788,6 +793,7 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
         case MSM_G1_PARAM_GROUPS: *value = c->groups; return MSM_G1_OK;
         case MSM_G1_PARAM_FINISH: *value = c->finish_t; return MSM_G1_OK;
         case MSM_G1_PARAM_GLV: *value = c->glv; return MSM_G1_OK;
+        case MSM_G1_PARAM_INVERSION: *value = c->inv_kind; return MSM_G1_OK;
         default: return MSM_G1_ERR_INVALID_ARG;
     }
 }
@@ -896,13 +902,14 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         launch_accum_level0(c->batch_s, c->tpb, resident, points, c->phi, nsplit, c->entries, c->offsets,
                             (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
-                            (terms * nw + (uint64_t)nw * B + 1) / 2, stats, s);
+                            (terms * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
         launches++;
     };
     auto tree = [&](int j, cudaStream_t s) {
         // levels while some bucket may still hold two items: 2^level < max bucket <= terms
         for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < terms; level++) {
-            launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, j, level, stats, s);
+            launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, j, level, stats,
+                               c->inv_kind, s);
             launches++;
         }
     };

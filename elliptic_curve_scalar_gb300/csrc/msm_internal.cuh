@@ -45,15 +45,17 @@ struct Resident {
 
 // accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32} is the
 // largest number of pairs a thread shares one inversion across
-// level 0 over the units of buckets [g0, g1); levels >= 1 over group grp's list
+// level 0 over the units of buckets [g0, g1); levels >= 1 over group grp's list;
+// inv_kind: 0 = safegcd, 1 = Fermat
 // (entry indices below nsplit address points, the others phi - nsplit)
 void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi,
                          uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, cudaStream_t st);
+                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st);
 void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
                         cudaStream_t st);
 void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, cudaStream_t st);
+                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                        cudaStream_t st);
 Resident accum_resident_threads(int tpb);
 // Jacobian sums of the buckets of [g0, g1) that left the tree with >= 2 items
 void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,

@@ -33,6 +33,7 @@ PARAM_STATS = 4
 PARAM_GROUPS = 5
 PARAM_FINISH = 6
 PARAM_GLV = 7
+PARAM_INVERSION = 8
 PLAIN_BITS = 255  # bits the signed windows of a scalar mod r cover
 GLV_BITS = 128    # bits the signed windows of one GLV half cover
 

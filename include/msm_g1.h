@@ -62,6 +62,8 @@ extern "C" {
 #define MSM_G1_PARAM_FINISH 6  /* buckets with at most T items leave the affine tree and are summed in
                                   Jacobian coordinates: T = 1..64, 1 = never, 0 = automatic (default) */
 #define MSM_G1_PARAM_GLV 7     /* 1: split every scalar by the curve endomorphism (default), 0: plain windows */
+#define MSM_G1_PARAM_INVERSION 8 /* field inversion of the batched additions: 0 = safegcd divsteps (default),
+                                    1 = Fermat a^(p-2) (slower; kept for comparison) */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 

@@ -182,6 +182,19 @@ def test_host_buffer_entry_edges():
     assert np.array_equal(normalise(out), oracle.closed_form(r[:100], k[:100]))
 
 
+@pytest.mark.parametrize("inversion", [1, 0])
+def test_inversion_choice(mid_case, inversion):
+    """Both batch inversions (safegcd divsteps, Fermat) give the oracle's result."""
+    pts, k, expect = mid_case
+    cx = ctx(20000, 13)
+    cx.set_param(gm.PARAM_INVERSION, inversion)
+    try:
+        got = normalise(cx.run(gpu_points(pts), gpu_scalars(k), 13))
+    finally:
+        cx.set_param(gm.PARAM_INVERSION, 0)
+    assert np.array_equal(got, expect)
+
+
 def test_empty_input():
     cx = ctx(16, 8)
     pts = torch.zeros((0, 16), dtype=torch.int32, device="cuda")
@@ -400,6 +413,18 @@ def test_config4_n2p22(big_points, c, glv):
     _, k = synth.uniform_workload(1 << 22, 1005)
     got = run_gpu(pts, k, c, max_n=1 << 22, max_c=18, glv=glv)
     assert np.array_equal(got, oracle.closed_form(r, k))
+
+
+def test_n2p23_beyond_the_configs(big_points):
+    """n = 2^23 (twice the largest configuration): the 2^22 points twice over,
+    with independent scalars; the closed form pins the result at any n."""
+    r, pts = big_points
+    _, k1 = synth.uniform_workload(1 << 22, 1007)
+    _, k2 = synth.uniform_workload(1 << 22, 1008)
+    r2 = np.concatenate([r, r])
+    k = np.concatenate([k1, k2])
+    got = run_gpu(np.concatenate([pts, pts]), k, 16, max_n=1 << 23, max_c=16)
+    assert np.array_equal(got, oracle.closed_form(r2, k))
 
 
 @pytest.mark.parametrize("glv", [1, 0])
