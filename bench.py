@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
     ap.add_argument("--glv", type=int, default=1, choices=[0, 1], help="split scalars by the GLV endomorphism")
     ap.add_argument("--inversion", type=int, default=0, choices=[0, 1], help="0: safegcd, 1: Fermat")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="K > 1: each step is K independent MSMs of the workload's size, fused by msm_g1_run_batch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -189,9 +191,11 @@ def run_gpu(args, cfg):
     dev = torch.device("cuda", local)
     n = cfg["n"]
     c = args.c or cfg["c"]
-    r, k = workload(cfg)
+    K = max(1, args.batch)
+    r, k = workload(dict(cfg, n=K * n))  # K independent MSMs of n terms each (K = 1: the plain MSM)
+    offsets = [i * n for i in range(K + 1)]
 
-    ctx = gm.MsmG1(n, c)
+    ctx = gm.MsmG1(K * n, c, max_batch=K)
     ctx.set_param(gm.PARAM_BATCH_S, args.batch_s)
     ctx.set_param(gm.PARAM_TPB, args.tpb)
     ctx.set_param(gm.PARAM_FINISH, args.finish)
@@ -201,7 +205,13 @@ def run_gpu(args, cfg):
     scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
     # points P_i = [r_i]G built on the device by the library's fixed-base kernel
     pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
-    out_d = torch.empty(24, dtype=torch.int32, device=dev)
+    out_d = torch.empty(24 * K, dtype=torch.int32, device=dev)
+
+    def msm(p_in, s_in):  # one step: the MSM, or the K fused MSMs of a batch
+        if K == 1:
+            ctx.run(p_in, s_in, c, out=out_d)
+        else:
+            ctx.run_batch(p_in, s_in, offsets, c, out=out_d.view(K, 24))
     torch.cuda.synchronize()
     pts_h = pts_d.cpu().pin_memory()
     scal_h = scal_d.cpu().pin_memory()
@@ -212,12 +222,12 @@ def run_gpu(args, cfg):
     # warm-up (also fixes the launch count and the exact work counters)
     ctx.set_param(gm.PARAM_STATS, 1)
     for _ in range(max(args.warmup, 3)):
-        ctx.run(pts_d, scal_d, c, out=out_d)
+        msm(pts_d, scal_d)
     stats = ctx.stats()
     nwin = -(-(gm.GLV_BITS if args.glv else gm.PLAIN_BITS) // c)
-    counts, _ = ctx.debug_read(0, nwin * (1 << (c - 1)))
+    counts, _ = ctx.debug_read(0, K * nwin * (1 << (c - 1)))
     ctx.set_param(gm.PARAM_STATS, 0)
-    ctx.run(pts_d, scal_d, c, out=out_d)
+    msm(pts_d, scal_d)
     launches_per_msm = int(ctx.stats()["launches"])
 
     uuid = None
@@ -237,7 +247,7 @@ def run_gpu(args, cfg):
     for s in range(args.steps):
         flush.zero_()  # evict the inputs from L2 (outside the step's events)
         starts[s].record(stream)
-        ctx.run(pts_d, scal_d, c, out=out_d)
+        msm(pts_d, scal_d)
         ends[s].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -249,7 +259,7 @@ def run_gpu(args, cfg):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * n * args.steps / (total_ms / 1000.0)
+    value = world * K * n * args.steps / (total_ms / 1000.0)
 
     # phase-timed steps: the serial schedule with CUDA events between phases on
     # the calling stream, which every kernel then runs on; the level-0 kernel's
@@ -258,7 +268,7 @@ def run_gpu(args, cfg):
     phases = []
     for s in range(min(args.steps, 50)):
         flush.zero_()
-        ctx.run(pts_d, scal_d, c, out=out_d)
+        msm(pts_d, scal_d)
         phases.append(ctx.phase_ms())
     ctx.set_param(gm.PARAM_TIMING, 0)
     clocks = sampler.stop()
@@ -268,13 +278,19 @@ def run_gpu(args, cfg):
     # runs the MSM and downloads the 96-byte result
     ctx.set_param(gm.PARAM_TIMING, 0)
     e2e_steps = args.steps
-    ctx.run_host(pts_h, scal_h, c, out=out_h)  # first call allocates the device copies
+    out_hk = torch.empty(24 * K, dtype=torch.int32).pin_memory()
+    if K == 1:
+        ctx.run_host(pts_h, scal_h, c, out=out_h)  # first call allocates the device copies
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        ctx.run_host(pts_h, scal_h, c, out=out_h)
+        if K == 1:
+            ctx.run_host(pts_h, scal_h, c, out=out_h)
+        else:  # no host-buffer batch entry: torch uploads, msm_g1_run_batch, torch download
+            msm(pts_h.to(dev, non_blocking=True), scal_h.to(dev, non_blocking=True))
+            out_hk.copy_(out_d, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -324,15 +340,16 @@ def run_gpu(args, cfg):
         line = {
             "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": (value / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) else None,
+            "vs_baseline": (value / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) and K == 1 else None,
             "dtype": "u32", "data": "synthetic",
-            "config": {"workload": "BN254 G1 MSM n=%d c=%d S=%d tpb=%d%s, %s points [r_i]G and scalars, seed %d"
-                                   % (n, c, args.batch_s, args.tpb, " GLV" if args.glv else "", cfg["kind"],
-                                      cfg["seed"]),
+            "config": {"workload": "BN254 G1 MSM %sn=%d c=%d S=%d tpb=%d%s, %s points [r_i]G and scalars, seed %d"
+                                   % ("%d fused x " % K if K > 1 else "", n, c, args.batch_s, args.tpb,
+                                      " GLV" if args.glv else "", cfg["kind"], cfg["seed"]),
                        "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"], "glv": args.glv,
+                       "batch": K,
                        "finish_t": args.finish or "auto", "groups": args.groups,
                        "l2": "flushed before every timed step (256 MiB write)", "replicas": world},
-            "ms_per_msm": ms_per_step,
+            "ms_per_msm": ms_per_step / K,
             "ms_median": statistics.median(step_ms),
             "phase_ms": mean_phase,
             "serial_ms_per_msm": round(sum(mean_phase.values()), 4),
@@ -349,9 +366,9 @@ def run_gpu(args, cfg):
                          "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,
-            "e2e": {"value": world * n / (e2e_ms / 1e3), "unit": "points/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": world * K * n / (e2e_ms / 1e3), "unit": "points/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": int(pts_h.numel() * 4 + scal_h.numel() * 4),
-                    "d2h_bytes_per_step": 96},
+                    "d2h_bytes_per_step": 96 * K},
             "gpu_launches": launches_per_msm * args.steps,
             "schedule": "timed steps: window groups pipelined over the library's streams; phase_ms and the roofline: serial phase-timed steps",
             "clocks": clocks,

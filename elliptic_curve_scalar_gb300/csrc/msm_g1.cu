@@ -49,6 +49,7 @@ constexpr int SCAN_TILE = SCAN_TPB * SCAN_ITEMS;
 constexpr int REDUCE_TPB = 256;
 constexpr uint32_t MAX_REDUCE_JOBS = 16;  // 1 + log2 G, G <= 2^12 (one warp per job)
 constexpr uint32_t REDUCE_MAX_PARTS = 8;  // partial blocks per reduction job
+constexpr uint64_t MAX_BATCH_WINDOWS = 4096;  // windows of all MSMs of one batch pass
 
 // ---------------------------------------------------------------- helpers
 
@@ -90,20 +91,39 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sm, ui
 // digits of |k1| go with point i, those of |k2| with point n + i (phi(P_i)),
 // each negated when its half is negative.  All lanes call f the same number
 // of times, so f may use warp collectives.
+// Batches: MSM m of a batch of `count` owns terms [off[m], off[m+1]) and the
+// windows [m W, (m + 1) W); the MSM of term i is found by binary search.
+struct BatchMap {
+    const uint32_t* off;  // count + 1 term offsets (device), or null for one MSM
+    int count;
+};
+
+__device__ __forceinline__ uint32_t msm_of(const BatchMap& bm, uint32_t i) {
+    if (!bm.off) return 0;
+    uint32_t lo = 0, hi = (uint32_t)bm.count;
+    while (hi - lo > 1) {  // the last m with off[m] <= i (empty MSMs are skipped)
+        const uint32_t mid = (lo + hi) >> 1;
+        if (__ldg(bm.off + mid) <= i) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
 template <bool GLV, class F>
 __device__ __forceinline__ void scalar_digits(const uint32_t* __restrict__ scalars, size_t n, size_t i, bool live,
-                                              int c, const Windows& L, F&& f) {
+                                              int c, const Windows& L, const BatchMap& bm, F&& f) {
     uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (live) {
         load_scalar(scalars + 8 * i, k);
         reduce_mod_r(k);
     }
     const uint32_t B = 1u << (c - 1);
+    const uint32_t wbase = live ? msm_of(bm, (uint32_t)i) * (uint32_t)L.W : 0;
     auto visit = [&](auto& half, uint32_t e_base, uint32_t neg) {
         uint32_t carry = 0;
         for (int w = 0; w < L.W; w++) {
             const int d = signed_digit(half, L, w, carry);
-            const uint32_t g = (live && d != 0) ? (uint32_t)w * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
+            const uint32_t g = (live && d != 0) ? (wbase + (uint32_t)w) * B + (uint32_t)(d < 0 ? -d : d) - 1u : HOLE;
             f(g, e_base | (((uint32_t)(d < 0) ^ neg) ? SIGN : 0u));
         }
     };
@@ -120,12 +140,12 @@ __device__ __forceinline__ void scalar_digits(const uint32_t* __restrict__ scala
 // One thread per scalar; the lanes of a warp hitting the same bucket share one
 // atomic.
 template <bool GLV>
-__global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L,
+__global__ void k_digits_hist(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L, BatchMap bm,
                               uint32_t* __restrict__ counts) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const bool live = i < n;
     const int lane = threadIdx.x & 31;
-    scalar_digits<GLV>(scalars, n, i, live, c, L, [&](uint32_t g, uint32_t) {
+    scalar_digits<GLV>(scalars, n, i, live, c, L, bm, [&](uint32_t g, uint32_t) {
         const uint32_t peers = __match_any_sync(0xffffffffu, g);
         if (g != HOLE && lane == __ffs(peers) - 1) atomicAdd(&counts[g], (uint32_t)__popc(peers));
     });
@@ -219,12 +239,12 @@ __global__ void k_scan_apply(const uint32_t* __restrict__ counts, uint32_t nb, c
 // ------------------------------------------------------------- 3. scatter
 
 template <bool GLV>
-__global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L,
+__global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c, Windows L, BatchMap bm,
                           uint32_t* __restrict__ cursor, uint32_t* __restrict__ entries) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    scalar_digits<GLV>(scalars, n, i, i < n, c, L, [&](uint32_t g, uint32_t e) {
+    scalar_digits<GLV>(scalars, n, i, i < n, c, L, bm, [&](uint32_t g, uint32_t e) {
         const uint32_t peers = __match_any_sync(0xffffffffu, g);
         const int leader = __ffs(peers) - 1;
         uint32_t pos = 0;
@@ -275,12 +295,12 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
 
 // Sum of the n Jacobian points in sm[0 .. n) (n a power of two, n <= blockDim.x
 // <= 256, one point per thread slot); the result lands in sm[0].  Wide levels
-// use one thread per addition; the last five (32 points down to 1) use a whole
-// warp per addition, whose latency is a third of one thread's.
+// use one thread per addition; once a level has at most one addition per warp,
+// a whole warp takes each addition (its latency is a third of one thread's).
 __device__ void block_tree_sum(uint32_t* sm, uint32_t n) {
     const uint32_t tid = threadIdx.x, warp = tid >> 5, nwarps = blockDim.x >> 5;
     uint32_t s = n;
-    for (; s > 32; s >>= 1) {
+    for (; (s >> 1) > nwarps; s >>= 1) {
         const uint32_t h = s >> 1;
         if (tid < h) g1::store_jac(sm + tid * 24, g1::add(g1::load_jac(sm + tid * 24), g1::load_jac(sm + (tid + h) * 24)));
         __syncthreads();
@@ -297,7 +317,8 @@ __device__ void block_tree_sum(uint32_t* sm, uint32_t n) {
 }
 
 // Job 0 of a window sums every C_j; job 1 + t sums the R_j with bit t of j set.
-// Block (w, job, part) sums the job's terms [part 256 m, (part + 1) 256 m), m per thread.
+// Block (w, job, part) of T threads (a power of two, 32 .. 256) sums the
+// job's terms [part T m, (part + 1) T m), m per thread.
 __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_jobs(const uint32_t* __restrict__ chunks, int w_lo, uint32_t G,
                                                             uint32_t jobs, uint32_t parts, uint32_t m,
                                                             uint32_t* __restrict__ partials) {
@@ -380,8 +401,21 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
 }
 
+// Batches: one warp per MSM m, Horner's rule over its windows [m W, (m + 1) W).
+__global__ void k_combine_batch(const uint32_t* __restrict__ wsums, Windows L, uint32_t* __restrict__ out) {
+    const uint32_t m = blockIdx.x;
+    const uint32_t* ws = wsums + (size_t)m * L.W * 24;
+    jac q = g1::load_jac(ws + (size_t)(L.W - 1) * 24);
+    for (int w = L.W - 2; w >= 0; w--) {
+        for (int i = window_width(L, w); i > 0; i--) q = g1c::dbl(q);
+        q = g1c::add(q, g1::load_jac(ws + (size_t)w * 24));
+    }
+    if (threadIdx.x == 0) g1::store_jac(out + (size_t)m * 24, q);
+}
+
+// infinity into out[blockIdx.x] (one block per result)
 __global__ void k_write_inf(uint32_t* out) {
-    if (threadIdx.x == 0) g1::store_jac(out, g1::jac_inf());
+    if (threadIdx.x == 0) g1::store_jac(out + (size_t)blockIdx.x * 24, g1::jac_inf());
 }
 
 // ------------------------------------------------------ generator multiples
@@ -434,6 +468,8 @@ struct msm_g1_ctx {
     char* scratch;
     uint32_t *counts, *offsets, *cursor, *tile_sums, *entries, *items, *chunks, *wsums, *gen_table, *gen_tj;
     uint32_t* partials;    // partial sums of the bucket-reduction jobs
+    uint32_t* msm_off;     // term offsets of the MSMs of a batch (device)
+    uint64_t cap_windows, cap_partials;
     uint32_t* pairs;
     uint32_t* qacc;        // running value of the window combination between groups
     uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
@@ -481,7 +517,7 @@ static uint32_t ilog2(uint32_t x) {
 // Reduction jobs of one window (sum of C_j, and one V_t per bit of the chunk
 // index) and their split into partial blocks of 256 threads x m terms.
 struct ReducePlan {
-    uint32_t L, G, jobs, parts, m;
+    uint32_t L, G, jobs, parts, m, tpb;
 };
 // m, the terms each thread adds before the block tree, is the smallest power
 // of two that keeps parts <= REDUCE_MAX_PARTS (a longer per-thread chain cost
@@ -492,14 +528,18 @@ static ReducePlan reduce_plan(uint32_t B) {
     r.G = B / r.L;
     r.jobs = 1 + ilog2(r.G);
     r.m = 1;
-    auto parts_for = [&](uint32_t m) { return (r.G + 256 * m - 1) / (256 * m); };
+    // blocks of the next power of two >= G threads, 32 .. 256: a small job
+    // (G = 32 at c = 8) would leave most of a 256-thread block adding infinities
+    r.tpb = 32;
+    while (r.tpb < 256 && r.tpb < r.G) r.tpb <<= 1;
+    auto parts_for = [&](uint32_t m) { return (r.G + r.tpb * m - 1) / (r.tpb * m); };
     while (parts_for(r.m) > REDUCE_MAX_PARTS) r.m <<= 1;
     r.parts = parts_for(r.m);
     return r;
 }
 
 struct sizing {
-    uint64_t points, entries, buckets, chunks, pairs, partials;
+    uint64_t points, entries, buckets, chunks, pairs, partials, windows;
 };
 
 // Level pair-list capacities for at most h_ub level-1 items in nb buckets:
@@ -547,8 +587,11 @@ static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_
     return lay;
 }
 
-static sizing size_for(size_t max_n, int max_c) {
-    sizing s{max_n, 0, 0, 0, 0, 0};
+// max_batch: MSMs fused in one pass (their per-bucket and per-window
+// buffers scale with it; max_n bounds the terms of the whole pass)
+static sizing size_for(size_t max_n, int max_c, int max_batch = 1) {
+    sizing s{max_n, 0, 0, 0, 0, 0, 0};
+    const uint64_t kb = (uint64_t)std::max(1, max_batch);
     // entries for windows down to 8 bits (smaller windows fit smaller n); the
     // GLV split doubles the terms and about halves the windows
     const int cmin = std::min(max_c, 8);
@@ -558,10 +601,11 @@ static sizing size_for(size_t max_n, int max_c) {
         uint64_t wb = (uint64_t)window_count(c) * B;
         const ReducePlan rp = reduce_plan((uint32_t)B);
         const uint64_t wg = (uint64_t)window_count(c) * rp.G;
-        s.buckets = std::max(s.buckets, wb);
-        s.chunks = std::max(s.chunks, wg);
-        s.partials = std::max(s.partials, (uint64_t)window_count(c) * rp.jobs * rp.parts);
+        s.buckets = std::max(s.buckets, wb * kb);
+        s.chunks = std::max(s.chunks, wg * kb);
+        s.partials = std::max(s.partials, (uint64_t)window_count(c) * rp.jobs * rp.parts * kb);
     }
+    s.windows = std::max<uint64_t>(256, std::min<uint64_t>(MAX_BATCH_WINDOWS, s.buckets));
     s.entries += s.buckets;  // one padding entry per bucket at most
     s.entries += 2;
     // pair lists: the largest grouped layout over the windows this context allows
@@ -572,6 +616,11 @@ static sizing size_for(size_t max_n, int max_c) {
             for (int groups = 1; groups <= MAX_GROUPS; groups++) {
                 uint64_t t = 0;
                 make_layout(terms, W, 1u << (c - 1), groups, &t);
+                s.pairs = std::max(s.pairs, t);
+            }
+            if (kb > 1) {  // a fused batch: one group over kb W windows
+                uint64_t t = 0;
+                make_layout((terms + kb - 1) / kb, (int)(W * kb), 1u << (c - 1), 1, &t);
                 s.pairs = std::max(s.pairs, t);
             }
         }
@@ -597,7 +646,8 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_items = take((size_t)64 * ((s.entries + 1) / 2));
     size_t o_chunks = take((size_t)192 * s.chunks);  // C_j, R_j per chunk
     size_t o_partials = take((size_t)96 * s.partials);
-    size_t o_wsums = take((size_t)96 * 256);
+    size_t o_wsums = take((size_t)96 * s.windows);
+    size_t o_msm_off = take((size_t)4 * (s.windows + 1));
     size_t o_table = take((size_t)64 * 256);
     size_t o_tj = take((size_t)96 * 256);
     size_t o_pairs = take((size_t)4 * s.pairs);
@@ -618,6 +668,7 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
         c->items = (uint32_t*)(c->scratch + o_items);
         c->chunks = (uint32_t*)(c->scratch + o_chunks);
         c->partials = (uint32_t*)(c->scratch + o_partials);
+        c->msm_off = (uint32_t*)(c->scratch + o_msm_off);
         c->wsums = (uint32_t*)(c->scratch + o_wsums);
         c->gen_table = (uint32_t*)(c->scratch + o_table);
         c->gen_tj = (uint32_t*)(c->scratch + o_tj);
@@ -647,6 +698,8 @@ int msm_g1_auto_window(size_t n) {
     return std::max(4, std::min(18, c));
 }
 
+int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) { return msm_g1_create_batch(out, max_n, max_c, 1); }
+
 size_t msm_g1_scratch_bytes(size_t max_n, int max_c) {
     if (max_n < 1 || max_c < 1 || max_c > MSM_G1_MAX_WINDOW) return 0;
     return layout(nullptr, size_for(max_n, max_c), false);
@@ -664,11 +717,12 @@ const char* msm_g1_strerror(int code) {
     }
 }
 
-int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
+int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch) {
     if (!out) return MSM_G1_ERR_INVALID_ARG;
     *out = nullptr;
     if (max_n < 1 || max_n > (1ull << 30) || max_c < 1 || max_c > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
-    sizing s = size_for(max_n, max_c);
+    if (max_batch < 1 || max_batch > (int)MAX_BATCH_WINDOWS) return MSM_G1_ERR_INVALID_ARG;
+    sizing s = size_for(max_n, max_c, max_batch);
     if (s.entries >= (1ull << 31) || s.pairs >= (1ull << 32)) return MSM_G1_ERR_INVALID_ARG;  // 32-bit offsets
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MSM_G1_ERR_NO_DEVICE;
@@ -684,6 +738,8 @@ int msm_g1_create(msm_g1_ctx** out, size_t max_n, int max_c) {
     c->cap_buckets = s.buckets;
     c->cap_chunks = s.chunks;
     c->cap_pairs = s.pairs;
+    c->cap_windows = s.windows;
+    c->cap_partials = s.partials;
     c->scratch_bytes = layout(nullptr, s, false);
     if (cudaMalloc((void**)&c->scratch, c->scratch_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -803,7 +859,8 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
 // The MSM.  points_host: when non-null, the points are copied from this host
 // buffer into `points` (device) on the side stream while the sort runs.
 static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
-                    uint32_t* out, cudaStream_t st, const uint32_t* points_host) {
+                    uint32_t* out, cudaStream_t st, const uint32_t* points_host, int count = 1,
+                    const uint32_t* d_off = nullptr) {
     int cw = window_c == 0 ? std::min(msm_g1_auto_window(n), c->max_c) : window_c;
     if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
     if (cw > c->max_c || n > c->max_n) return MSM_G1_ERR_CAPACITY;
@@ -814,8 +871,18 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     const uint64_t terms = glv ? 2 * (uint64_t)n : (uint64_t)n;
     const uint32_t nsplit = glv ? (uint32_t)n : HOLE;  // entry indices >= nsplit address phi
     const uint32_t B = 1u << (cw - 1);
-    const uint32_t nb = (uint32_t)W * B;
+    // a batch of `count` MSMs runs as one MSM over count W windows, MSM m
+    // owning windows [m W, (m + 1) W)
+    const int Wall = W * count;
+    const uint32_t nb = (uint32_t)Wall * B;
     if (terms * W + nb + 2 > c->cap_entries || nb > c->cap_buckets) return MSM_G1_ERR_CAPACITY;
+    {
+        const ReducePlan rp0 = reduce_plan(B);
+        if ((uint64_t)Wall > c->cap_windows || (uint64_t)Wall * rp0.G > c->cap_chunks ||
+            (uint64_t)Wall * rp0.jobs * rp0.parts > c->cap_partials)
+            return MSM_G1_ERR_CAPACITY;
+    }
+    const BatchMap bm{count > 1 ? d_off : nullptr, count};
     if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
     c->have_timing = false;
     if (c->timing && !c->events_made) {
@@ -827,7 +894,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     };
     if (n == 0) {
         CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
-        k_write_inf<<<1, 32, 0, st>>>(out);
+        k_write_inf<<<count, 32, 0, st>>>(out);
         c->last_launches = 1;
         return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
     }
@@ -859,8 +926,8 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
-        if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts);
-        else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->counts);
+        if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->counts);
+        else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->counts);
         launches++;
     }
     mark(1);
@@ -872,9 +939,12 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     // the phase events then delimit whole phases -- or when the context has no
     // streams of its own; otherwise window groups are pipelined (below).
     const int groups = c->groups ? c->groups : 2;  // two groups measured best (n = 2^16 .. 2^22)
-    const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1;
+    const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1 && count == 1;
     uint64_t pairs_total = 0;
-    PairLayout lay = make_layout(terms, W, B, pipelined ? groups : 1, &pairs_total);
+    // (a batch's windows hold only their own MSM's terms: ceil(terms / count)
+    // per window bounds the entries of all of them together)
+    const uint64_t terms_pw = (terms + count - 1) / count;
+    PairLayout lay = make_layout(terms_pw, Wall, B, pipelined ? groups : 1, &pairs_total);
     lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, c->resident[1].narrow));
     if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
@@ -882,8 +952,8 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     mark(2);
     {
         unsigned blocks = (unsigned)((n + 255) / 256);
-        if (glv) k_scatter<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->cursor, c->entries);
-        else k_scatter<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, c->cursor, c->entries);
+        if (glv) k_scatter<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->cursor, c->entries);
+        else k_scatter<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->cursor, c->entries);
         launches++;
     }
     mark(3);
@@ -902,7 +972,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         launch_accum_level0(c->batch_s, c->tpb, resident, points, c->phi, nsplit, c->entries, c->offsets,
                             (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
-                            (terms * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
+                            (terms_pw * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
         launches++;
     };
     auto tree = [&](int j, cudaStream_t s) {
@@ -923,14 +993,17 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         }
         k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum, lay.finish_t,
                                                              lay.w_lo[j], nw, B, L, G, c->chunks);
-        k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, REDUCE_TPB, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
-                                                                              rp.parts, rp.m, c->partials);
+        k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, rp.tpb, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
+                                                                          rp.parts, rp.m, c->partials);
         k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L), c->wsums);
         launches += 3;
     };
     auto combine = [&](int j, cudaStream_t s) {
-        k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
-                                        j == lay.groups - 1);
+        if (count > 1)  // one warp per MSM of the batch
+            k_combine_batch<<<count, 32, 0, s>>>(c->wsums, win, out);
+        else
+            k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
+                                            j == lay.groups - 1);
         launches++;
     };
     if (!pipelined) {
@@ -974,6 +1047,58 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
     if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
     if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
     return run_core(c, points, scalars, n, window_c, out, st, nullptr);
+}
+
+extern "C" int msm_g1_run_batch(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, const size_t* offsets,
+                                int count, int window_c, uint32_t* out, cudaStream_t st) {
+    if (!c || !out || !aligned16(out) || !offsets || count < 1) return MSM_G1_ERR_INVALID_ARG;
+    if (offsets[0] != 0) return MSM_G1_ERR_INVALID_ARG;
+    size_t largest = 0;
+    for (int m = 0; m < count; m++) {
+        if (offsets[m + 1] < offsets[m]) return MSM_G1_ERR_INVALID_ARG;
+        largest = std::max(largest, offsets[m + 1] - offsets[m]);
+    }
+    const size_t total = offsets[count];
+    if (total > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
+    if (largest > c->max_n) return MSM_G1_ERR_CAPACITY;
+    const int cw = window_c == 0 ? std::min(msm_g1_auto_window(largest), c->max_c) : window_c;
+    if (cw < 1 || cw > MSM_G1_MAX_WINDOW) return MSM_G1_ERR_INVALID_ARG;
+    if (cw > c->max_c) return MSM_G1_ERR_CAPACITY;
+    const int glv = c->glv != 0;
+    const int W = make_windows(cw, glv ? GLV_BITS : PLAIN_BITS).W;
+    const uint64_t B = 1ull << (cw - 1);
+    const ReducePlan rp = reduce_plan((uint32_t)B);
+    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
+    // Greedy passes: as many consecutive MSMs as the context's buffers hold.
+    int m0 = 0;
+    while (m0 < count) {
+        int cnt = 0;
+        uint64_t terms = 0;
+        while (m0 + cnt < count) {
+            const uint64_t t2 = terms + (offsets[m0 + cnt + 1] - offsets[m0 + cnt]);
+            const uint64_t k = (uint64_t)cnt + 1;
+            const uint64_t wall = k * W;
+            uint64_t pairs = 0;
+            make_layout(((t2 << glv) + k - 1) / k, (int)std::min<uint64_t>(wall, 1u << 30), (uint32_t)B, 1, &pairs);
+            const bool fits = t2 <= c->max_n && wall <= c->cap_windows && wall * B <= c->cap_buckets &&
+                              (t2 << glv) * W + wall * B + 2 <= c->cap_entries && wall * rp.G <= c->cap_chunks &&
+                              wall * rp.jobs * rp.parts <= c->cap_partials && pairs <= c->cap_pairs;
+            if (!fits) break;
+            terms = t2;
+            cnt++;
+        }
+        if (cnt == 0) return MSM_G1_ERR_CAPACITY;  // one MSM always fits a context made for it
+        uint32_t off[MAX_BATCH_WINDOWS + 1];
+        for (int m = 0; m <= cnt; m++) off[m] = (uint32_t)(offsets[m0 + m] - offsets[m0]);
+        // from pageable memory: the copy is staged before the call returns
+        CK(cudaMemcpyAsync(c->msm_off, off, 4ull * (cnt + 1), cudaMemcpyHostToDevice, st));
+        const size_t base = offsets[m0];
+        int rc = run_core(c, points ? points + 16 * base : nullptr, scalars ? scalars + 8 * base : nullptr, terms, cw,
+                          out + 24 * (size_t)m0, st, nullptr, cnt, c->msm_off);
+        if (rc != MSM_G1_OK) return rc;
+        m0 += cnt;
+    }
+    return MSM_G1_OK;
 }
 
 extern "C" int msm_g1_run_host(msm_g1_ctx* c, const uint32_t* points_host, const uint32_t* scalars_host, size_t n,
@@ -1127,6 +1252,8 @@ extern "C" int msm_g1_run_noalloc(const uint32_t* points, const uint32_t* scalar
     c.cap_buckets = s.buckets;
     c.cap_chunks = s.chunks;
     c.cap_pairs = s.pairs;
+    c.cap_windows = s.windows;
+    c.cap_partials = s.partials;
     c.scratch = (char*)g_noalloc_ptr[dev];
     c.scratch_bytes = NOALLOC_SCRATCH_BYTES;
     layout(&c, s, true);

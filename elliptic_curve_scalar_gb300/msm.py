@@ -49,9 +49,11 @@ _i = ctypes.c_int
 
 _SIGS = {
     "msm_g1_create": (_i, [ctypes.POINTER(_vp), _sz, _i]),
+    "msm_g1_create_batch": (_i, [ctypes.POINTER(_vp), _sz, _i, _i]),
     "msm_g1_run": (_i, [_vp, _vp, _vp, _sz, _i, _vp, _vp]),
     "msm_g1_run_noalloc": (_i, [_vp, _vp, _sz, _i, _vp, _vp]),
     "msm_g1_run_host": (_i, [_vp, _vp, _vp, _sz, _i, _vp, _vp]),
+    "msm_g1_run_batch": (_i, [_vp, _vp, _vp, ctypes.POINTER(_sz), _i, _i, _vp, _vp]),
     "msm_g1_mul_generator": (_i, [_vp, _vp, _sz, _vp, _vp]),
     "msm_g1_destroy": (None, [_vp]),
     "msm_g1_set_param": (_i, [_vp, _i, _i]),
@@ -151,13 +153,14 @@ def scratch_bytes(max_n, max_c):
 class MsmG1:
     """One MSM context: device scratch for n <= max_n and c <= max_c."""
 
-    def __init__(self, max_n, max_c=16, device=None):
+    def __init__(self, max_n, max_c=16, device=None, max_batch=1):
         self._ctx = ctypes.c_void_p()
         if not torch.cuda.is_available():
             raise MsmError(ERR_NO_DEVICE, "msm_g1_create")
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         with torch.cuda.device(self.device):
-            _check(lib().msm_g1_create(ctypes.byref(self._ctx), max_n, max_c), "msm_g1_create")
+            _check(lib().msm_g1_create_batch(ctypes.byref(self._ctx), max_n, max_c, max_batch),
+                   "msm_g1_create_batch")
         self.max_n = max_n
         self.max_c = max_c
 
@@ -199,6 +202,22 @@ class MsmG1:
         op = ctypes.c_void_p(out.data_ptr())
         with torch.cuda.device(self.device):
             _check(lib().msm_g1_run(self._ctx, pp, sp, n, c, op, _stream_handle(stream)), "msm_g1_run")
+        return out
+
+    def run_batch(self, points, scalars, offsets, c=0, out=None, stream=None):
+        """msm_g1_run_batch: len(offsets) - 1 MSMs over the concatenated terms;
+        returns a (count, 24) int32 tensor of Jacobian results (asynchronous)."""
+        count = len(offsets) - 1
+        if count < 1 or points.shape[0] != scalars.shape[0] or offsets[-1] != scalars.shape[0]:
+            raise ValueError("offsets must span the concatenated terms")
+        pp = _dev_u32(points, (16,), "points")
+        sp = _dev_u32(scalars, (8,), "scalars")
+        if out is None:
+            out = torch.empty((count, 24), dtype=torch.int32, device=points.device)
+        offs = (ctypes.c_size_t * (count + 1))(*[int(o) for o in offsets])
+        with torch.cuda.device(self.device):
+            _check(lib().msm_g1_run_batch(self._ctx, pp, sp, offs, count, c, ctypes.c_void_p(out.data_ptr()),
+                                          _stream_handle(stream)), "msm_g1_run_batch")
         return out
 
     def run_host(self, points, scalars, c=0, out=None, stream=None):

@@ -78,6 +78,13 @@ typedef struct msm_g1_ctx msm_g1_ctx;
  * allocation fails.  On error *ctx is set to NULL. */
 int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
 
+/* As msm_g1_create, with the per-bucket and per-window buffers sized for
+ * max_batch MSMs fused in one pass of msm_g1_run_batch (1 <= max_batch <=
+ * 4096); max_n then bounds the terms of a whole pass.  msm_g1_create(ctx, n,
+ * c) is msm_g1_create_batch(ctx, n, c, 1); a batch that does not fit one pass
+ * runs as several. */
+int msm_g1_create_batch(msm_g1_ctx **ctx, size_t max_n, int max_c, int max_batch);
+
 /* Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
  * With MSM_G1_PARAM_GLV = 1 (the default) each term is split by the
  * endomorphism phi(x, y) = (beta x, y) = [lambda](x, y) of BN254 G1 into
@@ -96,6 +103,20 @@ int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
  * call.  n = 0 writes infinity.  No host synchronisation. */
 int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
                int window_c, uint32_t *out_jacobian, cudaStream_t stream);
+
+/* A batch of count independent MSMs: out_jacobian[m] (24 uint32 each,
+ * device) = sum over terms i in [offsets[m], offsets[m+1]) of k_i * P_i.
+ * points_affine / scalars: device, the MSMs' terms concatenated (offsets[count]
+ * terms, layouts as for msm_g1_run); offsets: HOST array of count + 1
+ * nondecreasing term offsets with offsets[0] = 0 (empty MSMs give infinity).
+ * The MSMs run fused -- one sort, one accumulation pass, one reduction over
+ * the windows of all MSMs of a pass and one combination warp per MSM -- which
+ * is what makes many small MSMs cheap; a batch larger than the context's
+ * buffers is split into consecutive passes.  window_c applies to every MSM
+ * (0: chosen for the largest one).  Each MSM must have at most max_n terms.
+ * Asynchronous on stream; offsets may be reused as soon as the call returns. */
+int msm_g1_run_batch(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, const size_t *offsets,
+                     int count, int window_c, uint32_t *out_jacobian, cudaStream_t stream);
 
 /* The same MSM with inputs and output in HOST memory: points_affine (n x 16
  * uint32), scalars (n x 8 uint32) and out_jacobian (24 uint32), layouts as for

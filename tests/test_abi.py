@@ -77,6 +77,7 @@ def test_argument_checks_before_device_work(lib):
     """Null contexts and bad sizes are rejected on the host."""
     vp = ctypes.c_void_p
     assert lib.msm_g1_create(None, 16, 8) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_create_batch(None, 16, 8, 4) == gm.ERR_INVALID_ARG
     ctx = vp()
     assert lib.msm_g1_create(ctypes.byref(ctx), 16, 0) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_create(ctypes.byref(ctx), 0, 8) == gm.ERR_INVALID_ARG
@@ -84,6 +85,7 @@ def test_argument_checks_before_device_work(lib):
     assert not ctx.value
     assert lib.msm_g1_run(None, None, None, 0, 8, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_run_host(None, None, None, 0, 8, None, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_run_batch(None, None, None, None, 1, 8, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_set_param(None, gm.PARAM_BATCH_S, 8) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_mul_generator(None, None, 0, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_test_fq(99, None, None, None, 1, None) == gm.ERR_INVALID_ARG

@@ -6,6 +6,8 @@ Small and medium sizes are compared with oracle.msm directly; the full-size
 workloads (n = 2^20, 2^22) are compared with the closed form
 [sum_i k_i r_i mod r]G, which holds for any n because P_i = [r_i]G.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -193,6 +195,89 @@ def test_inversion_choice(mid_case, inversion):
     finally:
         cx.set_param(gm.PARAM_INVERSION, 0)
     assert np.array_equal(got, expect)
+
+
+def _batch_case(sizes, seed):
+    rs, ks = [], []
+    for i, n in enumerate(sizes):
+        r, k = synth.uniform_workload(n, seed + i) if n else (np.zeros((0, 4), np.uint64), np.zeros((0, 4), np.uint64))
+        rs.append(r)
+        ks.append(k)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    r_all = np.concatenate(rs)
+    return rs, ks, offsets, points_from_r(r_all), np.concatenate(ks)
+
+
+@pytest.mark.parametrize("glv", [1, 0])
+def test_batch_matches_each_msm(glv):
+    """msm_g1_run_batch: ragged and empty MSMs fused into one pass give each
+    MSM's own result (closed form) and the single-MSM entry's result."""
+    sizes = [700, 1, 0, 2500, 33, 1024, 0, 5]
+    rs, ks, offsets, pts, k = _batch_case(sizes, 8100)
+    cx = ctx(5000, 12)
+    cx.set_param(gm.PARAM_GLV, glv)
+    try:
+        out = cx.run_batch(gpu_points(pts), gpu_scalars(k), offsets, 9)
+        torch.cuda.synchronize()
+        for m, (r, km) in enumerate(zip(rs, ks)):
+            got = oracle.jacobian_mont_to_affine(gm.to_host(out[m]))
+            assert np.array_equal(got, oracle.closed_form(r, km)), m
+        single = normalise(cx.run(gpu_points(pts[offsets[3]:offsets[4]]), gpu_scalars(k[offsets[3]:offsets[4]]), 9))
+        assert np.array_equal(single, oracle.jacobian_mont_to_affine(gm.to_host(out[3])))
+    finally:
+        cx.set_param(gm.PARAM_GLV, 1)
+
+
+def test_batch_split_into_passes():
+    """A batch larger than the context's buffers runs as several passes:
+    200 MSMs at c = 13 need 2000 windows of 4096 buckets, more than a context
+    made for 4096 terms holds."""
+    sizes = [(37 * i) % 300 + 1 for i in range(200)]
+    rs, ks, offsets, pts, k = _batch_case(sizes, 8300)
+    cx = ctx(4096, 13)
+    out = cx.run_batch(gpu_points(pts), gpu_scalars(k), offsets, 13)
+    torch.cuda.synchronize()
+    for m in range(0, 200, 7):
+        got = oracle.jacobian_mont_to_affine(gm.to_host(out[m]))
+        assert np.array_equal(got, oracle.closed_form(rs[m], ks[m])), m
+    got = oracle.jacobian_mont_to_affine(gm.to_host(out[199]))
+    assert np.array_equal(got, oracle.closed_form(rs[199], ks[199]))
+
+
+def test_batch_context_fuses_one_pass():
+    """A context made for 16 fused MSMs (msm_g1_create_batch) runs 16 MSMs of
+    2^12 terms at c = 13 as one pass: one sort, one accumulation, one
+    reduction, 16 combination warps."""
+    sizes = [1 << 12] * 16
+    rs, ks, offsets, pts, k = _batch_case(sizes, 8500)
+    with gm.MsmG1(1 << 16, 13, max_batch=16) as cx:
+        out = cx.run_batch(gpu_points(pts), gpu_scalars(k), offsets, 13)
+        torch.cuda.synchronize()
+        for m in range(16):
+            got = oracle.jacobian_mont_to_affine(gm.to_host(out[m]))
+            assert np.array_equal(got, oracle.closed_form(rs[m], ks[m])), m
+    with gm.MsmG1(1 << 16, 13) as cx1:  # sized for one MSM: several passes, same points
+        out1 = cx1.run_batch(gpu_points(pts), gpu_scalars(k), offsets, 13)
+        torch.cuda.synchronize()
+        for m in (0, 7, 15):
+            assert np.array_equal(oracle.jacobian_mont_to_affine(gm.to_host(out1[m])),
+                                  oracle.jacobian_mont_to_affine(gm.to_host(out[m])))
+
+
+def test_batch_argument_errors():
+    cx = ctx(100, 8)
+    r, k = synth.uniform_workload(120, 3)
+    pts, ks = gpu_points(points_from_r(r)), gpu_scalars(k)
+    with pytest.raises(gm.MsmError) as e:
+        cx.run_batch(pts, ks, [0, 120], 8)  # one MSM beyond max_n
+    assert e.value.code == gm.ERR_CAPACITY
+    out = cx.run_batch(pts, ks, [0, 60, 120], 8)  # two that fit
+    torch.cuda.synchronize()
+    assert np.array_equal(oracle.jacobian_mont_to_affine(gm.to_host(out[1])), oracle.closed_form(r[60:], k[60:]))
+    lib = gm.lib()
+    bad = (ctypes.c_size_t * 3)(0, 80, 60)  # decreasing offsets
+    assert lib.msm_g1_run_batch(cx._ctx, ctypes.c_void_p(pts.data_ptr()), ctypes.c_void_p(ks.data_ptr()), bad, 2, 8,
+                                ctypes.c_void_p(out.data_ptr()), None) == gm.ERR_INVALID_ARG
 
 
 def test_empty_input():
