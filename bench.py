@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="n2p16", choices=sorted(CONFIGS))
     ap.add_argument("--c", type=int, default=0, help="override the window size")
-    ap.add_argument("--batch-s", type=int, default=32)
+    ap.add_argument("--batch-s", type=int, default=0,
+                    help="additions per inversion: 1..64, 0 = the library's per-launch choice (32 or 64)")
     ap.add_argument("--tpb", type=int, default=128)
     ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
@@ -323,7 +324,7 @@ def run_gpu(args, cfg):
         try:
             with open(prof) as f:
                 tj = json.load(f)
-            key = "%s_S%d" % (args.config, args.batch_s)
+            key = "%s_S%s" % (args.config, args.batch_s or "auto")
             traffic = tj.get(key)
         except (OSError, ValueError):
             traffic = None
@@ -342,10 +343,10 @@ def run_gpu(args, cfg):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": (value / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) and K == 1 else None,
             "dtype": "u32", "data": "synthetic",
-            "config": {"workload": "BN254 G1 MSM %sn=%d c=%d S=%d tpb=%d%s, %s points [r_i]G and scalars, seed %d"
-                                   % ("%d fused x " % K if K > 1 else "", n, c, args.batch_s, args.tpb,
+            "config": {"workload": "BN254 G1 MSM %sn=%d c=%d S=%s tpb=%d%s, %s points [r_i]G and scalars, seed %d"
+                                   % ("%d fused x " % K if K > 1 else "", n, c, args.batch_s or "auto", args.tpb,
                                       " GLV" if args.glv else "", cfg["kind"], cfg["seed"]),
-                       "n": n, "c": c, "S": args.batch_s, "tpb": args.tpb, "kind": cfg["kind"], "glv": args.glv,
+                       "n": n, "c": c, "S": args.batch_s or "auto", "tpb": args.tpb, "kind": cfg["kind"], "glv": args.glv,
                        "batch": K,
                        "finish_t": args.finish or "auto", "groups": args.groups,
                        "l2": "flushed before every timed step (256 MiB write)", "replicas": world},
@@ -361,8 +362,9 @@ def run_gpu(args, cfg):
                          "count_basis": "6 Fq muls per addition x 264 IMAD slots per mul (128 full limb products at 2 slots + 8 low; inversion excluded)",
                          "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
-                         "inversion": "%s, one per %d additions" % (
-                             "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)", args.batch_s),
+                         "inversion": "%s, one per %s additions" % (
+                             "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)",
+                             args.batch_s or "S (32 or 64 per launch)"),
                          "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,

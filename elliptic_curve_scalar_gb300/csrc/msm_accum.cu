@@ -281,6 +281,15 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
 // the register-capped build once the work fills a resident wave of the other
 static bool wide(uint64_t work, int S, const Resident& res) { return (work + S - 1) / S >= res.narrow; }
 
+// batch_s = 0 (automatic): batches of 64 once they fill two resident waves of
+// the capped build -- half the inversions per addition of 32 (n = 2^22:
+// 12.59 -> 12.24 ms) -- else 32, which keeps the last wave of a launch of
+// one or two waves from running nearly empty (n = 2^20 was 1 % slower at 64)
+static int auto_batch(int batch_s, uint64_t work, const Resident& res) {
+    if (batch_s) return batch_s;
+    return (work + 63) / 64 >= 2 * res.wide ? 64 : 32;
+}
+
 template <int S>
 static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
                      const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
@@ -309,12 +318,13 @@ void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32
                          uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
 #define L0(S) \
     level0_t<S>(tpb, res, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, inv_kind, st)
-    switch (batch_s) {
+    switch (auto_batch(batch_s, units_ub, res)) {
         case 1: L0(1); break;
         case 2: L0(2); break;
         case 4: L0(4); break;
         case 8: L0(8); break;
         case 16: L0(16); break;
+        case 64: L0(64); break;
         default: L0(32); break;
     }
 #undef L0
@@ -331,12 +341,13 @@ void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* ite
     const uint32_t* list = pairs + lay.base[grp][level];
     uint64_t cap = lay.cap[grp][level];
 #define LV(S) list_t<S>(tpb, res, items, list, ctl, cap, grp, level, stats, inv_kind, st)
-    switch (batch_s) {
+    switch (auto_batch(batch_s, cap, res)) {
         case 1: LV(1); break;
         case 2: LV(2); break;
         case 4: LV(4); break;
         case 8: LV(8); break;
         case 16: LV(16); break;
+        case 64: LV(64); break;
         default: LV(32); break;
     }
 #undef LV

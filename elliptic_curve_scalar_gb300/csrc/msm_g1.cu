@@ -747,7 +747,7 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
         return MSM_G1_ERR_ALLOC;
     }
     layout(c, s, true);
-    c->batch_s = 32;
+    c->batch_s = 0;
     c->tpb = 128;
     c->timing = 0;
     c->glv = 1;
@@ -802,7 +802,8 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
     if (!c) return MSM_G1_ERR_INVALID_ARG;
     switch (key) {
         case MSM_G1_PARAM_BATCH_S:
-            if (value != 1 && value != 2 && value != 4 && value != 8 && value != 16 && value != 32)
+            if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8 && value != 16 && value != 32 &&
+                value != 64)
                 return MSM_G1_ERR_INVALID_ARG;
             c->batch_s = value;
             return MSM_G1_OK;
@@ -1257,7 +1258,7 @@ extern "C" int msm_g1_run_noalloc(const uint32_t* points, const uint32_t* scalar
     c.scratch = (char*)g_noalloc_ptr[dev];
     c.scratch_bytes = NOALLOC_SCRATCH_BYTES;
     layout(&c, s, true);
-    c.batch_s = 32;
+    c.batch_s = 0;
     c.tpb = 128;
     c.glv = 1;
     for (int i = 0; i < 3; i++) c.resident[i] = g_noalloc_resident[dev][i];

@@ -43,7 +43,8 @@ struct Resident {
     uint64_t narrow, wide;
 };
 
-// accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32} is the
+// accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32, 64} (0: chosen
+// per launch) is the
 // largest number of pairs a thread shares one inversion across
 // level 0 over the units of buckets [g0, g1); levels >= 1 over group grp's list;
 // inv_kind: 0 = safegcd, 1 = Fermat

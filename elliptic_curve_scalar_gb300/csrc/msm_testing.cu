@@ -148,7 +148,7 @@ extern "C" int msm_g1_test_batch_add(const uint32_t* a, const uint32_t* b, uint3
         else                                                                                     \
             k_test_batch_add<S, false><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n); \
         break;
-        CASE(1) CASE(2) CASE(4) CASE(8) CASE(16) CASE(32)
+        CASE(1) CASE(2) CASE(4) CASE(8) CASE(16) CASE(32) CASE(64)
 #undef CASE
         default: return MSM_G1_ERR_INVALID_ARG;
     }

@@ -54,7 +54,8 @@ extern "C" {
 #define MSM_G1_MAX_WINDOW 20
 
 /* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
-#define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32 (default 32) */
+#define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32, 64,
+                                  or 0 = per launch (default): 64 where such batches fill two resident waves, else 32 */
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */

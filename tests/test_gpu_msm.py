@@ -30,7 +30,7 @@ def ctx(max_n, max_c):
     return _ctx[key]
 
 
-def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=32, tpb=128, glv=1):
+def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=0, tpb=128, glv=1):
     n = k.shape[0]
     cx = ctx(max_n or max(n, 1), max_c or max(c, 1))
     cx.set_param(gm.PARAM_BATCH_S, batch_s)
@@ -81,7 +81,7 @@ def mid_case():
     return pts, k, expect_oracle(pts, k)
 
 
-@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("batch_s", [0, 1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("tpb", [64, 128, 256])
 def test_knobs(mid_case, batch_s, tpb):
     """Every batch size S and block size gives the same result (the pages
@@ -483,7 +483,7 @@ def test_config2_n65536_c13(big_points, glv):
     assert np.array_equal(got, oracle.closed_form(r, k))
 
 
-@pytest.mark.parametrize("batch_s", [4, 8, 16, 32])
+@pytest.mark.parametrize("batch_s", [0, 4, 8, 16, 32, 64])
 def test_config3_n2p20_c16(big_points, batch_s):
     r_all, pts_all = big_points
     n = 1 << 20

@@ -85,7 +85,7 @@ def test_jacobian_ops():
 
 
 @pytest.mark.parametrize("inline_back", [0, 1])
-@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32, 64])
 def test_batch_affine_add(batch_s, inline_back):
     """Batched affine pair additions, including pairs that would poison a
     shared inversion: equal points (tangent), opposite points, infinity."""
