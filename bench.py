@@ -56,7 +56,11 @@ PAGES_MS_LOGN16 = 50.0
 # Montgomery multiplication can issue on this pipe.
 IMAD_SLOTS_PER_CLK_PER_SM = 64
 IMAD_SLOTS_PER_FQ_MUL = 2 * 128 + 8
-FQ_MULS_PER_ADD = 6  # 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
+# A squaring needs 28 off-diagonal + 8 diagonal full products and the 8 low
+# products of the reduction: 2 * (36 + 64) + 8 = 208 slots.
+IMAD_SLOTS_PER_FQ_SQR = 2 * (36 + 64) + 8
+# 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
+IMAD_SLOTS_PER_ADD = 5 * IMAD_SLOTS_PER_FQ_MUL + IMAD_SLOTS_PER_FQ_SQR
 
 
 def parse():
@@ -316,7 +320,7 @@ def run_gpu(args, cfg):
         pass
     sm_max_mhz = peaks.get("sm_max_mhz", 2070.0)
     peak_timad = sms * IMAD_SLOTS_PER_CLK_PER_SM * sm_max_mhz * 1e6 / 1e12
-    strict_imad = adds_l0 * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
+    strict_imad = adds_l0 * IMAD_SLOTS_PER_ADD
     achieved = strict_imad / (l0_ms / 1e3) / 1e12
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
@@ -359,13 +363,13 @@ def run_gpu(args, cfg):
                          "kernel": "k_accum_level0",
                          "peak_basis": "%d SMs x %d IMAD slots/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
                                        % (sms, IMAD_SLOTS_PER_CLK_PER_SM, sm_max_mhz),
-                         "count_basis": "6 Fq muls per addition x 264 IMAD slots per mul (128 full limb products at 2 slots + 8 low; inversion excluded)",
+                         "count_basis": "5 Fq muls x 264 IMAD slots (128 full limb products at 2 slots + 8 low) + 1 squaring x 208 slots (36 + 64 full products + 8 low) per addition = 1528; inversion excluded",
                          "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
                          "inversion": "%s, one per %s additions" % (
                              "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)",
                              args.batch_s or "S (32 or 64 per launch)"),
-                         "accumulation_frac_all_levels": adds_total * FQ_MULS_PER_ADD * IMAD_SLOTS_PER_FQ_MUL
+                         "accumulation_frac_all_levels": adds_total * IMAD_SLOTS_PER_ADD
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,
             "e2e": {"value": world * K * n / (e2e_ms / 1e3), "unit": "points/s", "ms_per_step": e2e_ms,

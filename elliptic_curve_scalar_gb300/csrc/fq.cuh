@@ -227,6 +227,154 @@ __device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
     return r;
 }
 
+// a^2 * R^-1 mod p.  The 512-bit square is 2 (sum over i < j of a_i a_j
+// 2^(32 (i + j))) + sum a_i^2 2^(64 i): seven triangular rows of the 28
+// off-diagonal products (row i: a_i a_j for j > i, at limb 2i + 1 on, in two
+// fused-pair chains like mac_row -- the even and the odd j -- each rippling its
+// carry to the row's top limb i + 9, which no earlier row has reached), one
+// doubling carry chain, and one chain of the 8 diagonal products as fused pairs
+// at limbs (2i, 2i + 1).  36 limb products instead of 64: 208 issue slots of the
+// multiply pipe instead of 264.  The Montgomery rounds are those of mul_inline.
+__device__ __forceinline__ fe sqr_inline(const fe& a) {
+    uint32_t T[17];
+#pragma unroll
+    for (int i = 0; i < 17; i++) T[i] = 0;
+    asm("mad.lo.cc.u32 %0, %9, %10, %0;\n\t"
+        "madc.hi.cc.u32 %1, %9, %10, %1;\n\t"
+        "madc.lo.cc.u32 %2, %9, %12, %2;\n\t"
+        "madc.hi.cc.u32 %3, %9, %12, %3;\n\t"
+        "madc.lo.cc.u32 %4, %9, %14, %4;\n\t"
+        "madc.hi.cc.u32 %5, %9, %14, %5;\n\t"
+        "madc.lo.cc.u32 %6, %9, %16, %6;\n\t"
+        "madc.hi.cc.u32 %7, %9, %16, %7;\n\t"
+        "addc.u32 %8, %8, 0;\n\t"
+        "mad.lo.cc.u32 %1, %9, %11, %1;\n\t"
+        "madc.hi.cc.u32 %2, %9, %11, %2;\n\t"
+        "madc.lo.cc.u32 %3, %9, %13, %3;\n\t"
+        "madc.hi.cc.u32 %4, %9, %13, %4;\n\t"
+        "madc.lo.cc.u32 %5, %9, %15, %5;\n\t"
+        "madc.hi.cc.u32 %6, %9, %15, %6;\n\t"
+        "addc.cc.u32 %7, %7, 0;\n\t"
+        "addc.u32 %8, %8, 0;\n\t"
+        : "+r"(T[1]), "+r"(T[2]), "+r"(T[3]), "+r"(T[4]), "+r"(T[5]), "+r"(T[6]), "+r"(T[7]), "+r"(T[8]), "+r"(T[9])
+        : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %8, %9, %0;\n\t"
+        "madc.hi.cc.u32 %1, %8, %9, %1;\n\t"
+        "madc.lo.cc.u32 %2, %8, %11, %2;\n\t"
+        "madc.hi.cc.u32 %3, %8, %11, %3;\n\t"
+        "madc.lo.cc.u32 %4, %8, %13, %4;\n\t"
+        "madc.hi.cc.u32 %5, %8, %13, %5;\n\t"
+        "addc.cc.u32 %6, %6, 0;\n\t"
+        "addc.u32 %7, %7, 0;\n\t"
+        "mad.lo.cc.u32 %1, %8, %10, %1;\n\t"
+        "madc.hi.cc.u32 %2, %8, %10, %2;\n\t"
+        "madc.lo.cc.u32 %3, %8, %12, %3;\n\t"
+        "madc.hi.cc.u32 %4, %8, %12, %4;\n\t"
+        "madc.lo.cc.u32 %5, %8, %14, %5;\n\t"
+        "madc.hi.cc.u32 %6, %8, %14, %6;\n\t"
+        "addc.u32 %7, %7, 0;\n\t"
+        : "+r"(T[3]), "+r"(T[4]), "+r"(T[5]), "+r"(T[6]), "+r"(T[7]), "+r"(T[8]), "+r"(T[9]), "+r"(T[10])
+        : "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %7, %8, %0;\n\t"
+        "madc.hi.cc.u32 %1, %7, %8, %1;\n\t"
+        "madc.lo.cc.u32 %2, %7, %10, %2;\n\t"
+        "madc.hi.cc.u32 %3, %7, %10, %3;\n\t"
+        "madc.lo.cc.u32 %4, %7, %12, %4;\n\t"
+        "madc.hi.cc.u32 %5, %7, %12, %5;\n\t"
+        "addc.u32 %6, %6, 0;\n\t"
+        "mad.lo.cc.u32 %1, %7, %9, %1;\n\t"
+        "madc.hi.cc.u32 %2, %7, %9, %2;\n\t"
+        "madc.lo.cc.u32 %3, %7, %11, %3;\n\t"
+        "madc.hi.cc.u32 %4, %7, %11, %4;\n\t"
+        "addc.cc.u32 %5, %5, 0;\n\t"
+        "addc.u32 %6, %6, 0;\n\t"
+        : "+r"(T[5]), "+r"(T[6]), "+r"(T[7]), "+r"(T[8]), "+r"(T[9]), "+r"(T[10]), "+r"(T[11])
+        : "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %6, %7, %0;\n\t"
+        "madc.hi.cc.u32 %1, %6, %7, %1;\n\t"
+        "madc.lo.cc.u32 %2, %6, %9, %2;\n\t"
+        "madc.hi.cc.u32 %3, %6, %9, %3;\n\t"
+        "addc.cc.u32 %4, %4, 0;\n\t"
+        "addc.u32 %5, %5, 0;\n\t"
+        "mad.lo.cc.u32 %1, %6, %8, %1;\n\t"
+        "madc.hi.cc.u32 %2, %6, %8, %2;\n\t"
+        "madc.lo.cc.u32 %3, %6, %10, %3;\n\t"
+        "madc.hi.cc.u32 %4, %6, %10, %4;\n\t"
+        "addc.u32 %5, %5, 0;\n\t"
+        : "+r"(T[7]), "+r"(T[8]), "+r"(T[9]), "+r"(T[10]), "+r"(T[11]), "+r"(T[12])
+        : "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %5, %6, %0;\n\t"
+        "madc.hi.cc.u32 %1, %5, %6, %1;\n\t"
+        "madc.lo.cc.u32 %2, %5, %8, %2;\n\t"
+        "madc.hi.cc.u32 %3, %5, %8, %3;\n\t"
+        "addc.u32 %4, %4, 0;\n\t"
+        "mad.lo.cc.u32 %1, %5, %7, %1;\n\t"
+        "madc.hi.cc.u32 %2, %5, %7, %2;\n\t"
+        "addc.cc.u32 %3, %3, 0;\n\t"
+        "addc.u32 %4, %4, 0;\n\t"
+        : "+r"(T[9]), "+r"(T[10]), "+r"(T[11]), "+r"(T[12]), "+r"(T[13])
+        : "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %4, %5, %0;\n\t"
+        "madc.hi.cc.u32 %1, %4, %5, %1;\n\t"
+        "addc.cc.u32 %2, %2, 0;\n\t"
+        "addc.u32 %3, %3, 0;\n\t"
+        "mad.lo.cc.u32 %1, %4, %6, %1;\n\t"
+        "madc.hi.cc.u32 %2, %4, %6, %2;\n\t"
+        "addc.u32 %3, %3, 0;\n\t"
+        : "+r"(T[11]), "+r"(T[12]), "+r"(T[13]), "+r"(T[14])
+        : "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\t"
+        "madc.hi.cc.u32 %1, %3, %4, %1;\n\t"
+        "addc.u32 %2, %2, 0;\n\t"
+        : "+r"(T[13]), "+r"(T[14]), "+r"(T[15])
+        : "r"(a.v[6]), "r"(a.v[7]));
+    // T = 2 T (the off-diagonal sum is below 2^510)
+    asm("add.cc.u32  %0, %0, %0;\n\t"
+        "addc.cc.u32 %1, %1, %1;\n\t"
+        "addc.cc.u32 %2, %2, %2;\n\t"
+        "addc.cc.u32 %3, %3, %3;\n\t"
+        "addc.cc.u32 %4, %4, %4;\n\t"
+        "addc.cc.u32 %5, %5, %5;\n\t"
+        "addc.cc.u32 %6, %6, %6;\n\t"
+        "addc.cc.u32 %7, %7, %7;\n\t"
+        "addc.cc.u32 %8, %8, %8;\n\t"
+        "addc.cc.u32 %9, %9, %9;\n\t"
+        "addc.cc.u32 %10, %10, %10;\n\t"
+        "addc.cc.u32 %11, %11, %11;\n\t"
+        "addc.cc.u32 %12, %12, %12;\n\t"
+        "addc.cc.u32 %13, %13, %13;\n\t"
+        "addc.cc.u32 %14, %14, %14;\n\t"
+        "addc.u32    %15, %15, %15;"
+        : "+r"(T[0]), "+r"(T[1]), "+r"(T[2]), "+r"(T[3]), "+r"(T[4]), "+r"(T[5]), "+r"(T[6]), "+r"(T[7]), "+r"(T[8]), "+r"(T[9]), "+r"(T[10]), "+r"(T[11]), "+r"(T[12]), "+r"(T[13]), "+r"(T[14]), "+r"(T[15]));
+    // T += sum_i a_i^2 2^(64 i); the square is below 2^512, no carry out
+    asm("mad.lo.cc.u32  %0, %16, %16, %0;\n\t"
+        "madc.hi.cc.u32 %1, %16, %16, %1;\n\t"
+        "madc.lo.cc.u32 %2, %17, %17, %2;\n\t"
+        "madc.hi.cc.u32 %3, %17, %17, %3;\n\t"
+        "madc.lo.cc.u32 %4, %18, %18, %4;\n\t"
+        "madc.hi.cc.u32 %5, %18, %18, %5;\n\t"
+        "madc.lo.cc.u32 %6, %19, %19, %6;\n\t"
+        "madc.hi.cc.u32 %7, %19, %19, %7;\n\t"
+        "madc.lo.cc.u32 %8, %20, %20, %8;\n\t"
+        "madc.hi.cc.u32 %9, %20, %20, %9;\n\t"
+        "madc.lo.cc.u32 %10, %21, %21, %10;\n\t"
+        "madc.hi.cc.u32 %11, %21, %21, %11;\n\t"
+        "madc.lo.cc.u32 %12, %22, %22, %12;\n\t"
+        "madc.hi.cc.u32 %13, %22, %22, %13;\n\t"
+        "madc.lo.cc.u32 %14, %23, %23, %14;\n\t"
+        "madc.hi.u32    %15, %23, %23, %15;"
+        : "+r"(T[0]), "+r"(T[1]), "+r"(T[2]), "+r"(T[3]), "+r"(T[4]), "+r"(T[5]), "+r"(T[6]), "+r"(T[7]), "+r"(T[8]), "+r"(T[9]), "+r"(T[10]), "+r"(T[11]), "+r"(T[12]), "+r"(T[13]), "+r"(T[14]), "+r"(T[15])
+        : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]), "r"(a.v[6]), "r"(a.v[7]));
+    uint32_t cin = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) mac_row_p(T + i, cin, T[i] * FQ_NP0);
+    fe r;
+#pragma unroll
+    for (int j = 0; j < 8; j++) r.v[j] = T[8 + j];
+    reduce_once(r);
+    return r;
+}
+
 // Called, not inlined: every kernel of the MSM runs long sequences of field
 // multiplications, and inlining each ~330-instruction body at every call site
 // makes the hot loops overflow the per-sub-partition instruction cache (the
@@ -235,6 +383,13 @@ __device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
 // makes the caller store the operand to its stack frame and the callee load it
 // back, two round trips through local memory per multiplication.
 static __device__ __noinline__ fe mul(fe a, fe b) { return mul_inline(a, b); }
+
+// sqr_fused (called, like mul) issues fewer multiply-pipe slots but its three
+// chains (rows, doubling, diagonal) are more serial than a multiplication's
+// rows: it pays in the throughput-bound batched additions (n = 2^22: tree
+// levels 5.72 -> 5.58 ms) and costs in the latency-bound Jacobian chains of the
+// bucket reduction (0.49 -> 0.53 ms), which therefore square by multiplying.
+static __device__ __noinline__ fe sqr_fused(fe a) { return sqr_inline(a); }
 
 __device__ __forceinline__ fe sqr(const fe& a) { return mul(a, a); }
 

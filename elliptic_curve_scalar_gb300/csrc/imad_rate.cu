@@ -148,15 +148,25 @@ __global__ void k_mul_lat(const uint32_t* in, uint32_t* out, int iters, long lon
     cyc[0] = t1 - t0;
 }
 
+template <bool SQR>
 __global__ void k_mul_tput(const uint32_t* in, uint32_t* out, int iters) {
     fe x0 = fq::load(in), x1 = fq::load(in), y = fq::load(in + 8);
     x0.v[0] ^= threadIdx.x;
     x1.v[0] ^= threadIdx.x + 1;
     for (int i = 0; i < iters; i++) {
-        x0 = fq::mul(x0, y);
-        x1 = fq::mul(x1, y);
+        x0 = SQR ? fq::sqr_fused(x0) : fq::mul(x0, y);
+        x1 = SQR ? fq::sqr_fused(x1) : fq::mul(x1, y);
     }
     fq::store(out + 8 * (blockIdx.x * blockDim.x + threadIdx.x), fq::add(x0, x1));
+}
+
+__global__ void k_sqr_lat(const uint32_t* in, uint32_t* out, int iters, long long* cyc) {
+    fe x = fq::load(in);
+    long long t0 = clock64();
+    for (int i = 0; i < iters; i++) x = fq::sqr_fused(x);
+    long long t1 = clock64();
+    fq::store(out, x);
+    cyc[0] = t1 - t0;
 }
 
 int main() {
@@ -222,15 +232,25 @@ int main() {
     CK(cudaMemcpy(&cyc, d_cyc, 8, cudaMemcpyDeviceToHost));
     printf("fq::mul latency: %.1f cycles\n", (double)cyc / 2000);
     const int mb = sms * 16, mt = 128, mit = 256;
-    k_mul_tput<<<mb, mt>>>(d_in, d_out, 8);
+    k_mul_tput<false><<<mb, mt>>>(d_in, d_out, 8);
     cudaEventRecord(e0);
-    k_mul_tput<<<mb, mt>>>(d_in, d_out, mit);
+    k_mul_tput<false><<<mb, mt>>>(d_in, d_out, mit);
     cudaEventRecord(e1);
     CK(cudaEventSynchronize(e1));
     cudaEventElapsedTime(&ms, e0, e1);
     double muls = (double)mb * mt * mit * 2;
     printf("fq::mul throughput: %.2f Gmul/s = %.2f T IMAD slots/s (264 slots per mul)\n", muls / (ms * 1e-3) / 1e9,
            muls * 264 / (ms * 1e-3) / 1e12);
+    cudaEventRecord(e0);
+    k_mul_tput<true><<<mb, mt>>>(d_in, d_out, mit);
+    cudaEventRecord(e1);
+    CK(cudaEventSynchronize(e1));
+    cudaEventElapsedTime(&ms, e0, e1);
+    printf("fq::sqr_fused throughput: %.2f Gsqr/s = %.2f T IMAD slots/s (208 slots per squaring)\n",
+           muls / (ms * 1e-3) / 1e9, muls * 208 / (ms * 1e-3) / 1e12);
+    k_sqr_lat<<<1, 1>>>(d_in, d_out, 2000, d_cyc);
+    CK(cudaMemcpy(&cyc, d_cyc, 8, cudaMemcpyDeviceToHost));
+    printf("fq::sqr_fused latency: %.1f cycles\n", (double)cyc / 2000);
     CK(cudaGetLastError());
     return 0;
 }

@@ -181,13 +181,13 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
         num = fq::sub(q.y, p.y);
         x2 = q.x;
     } else {  // tangent: 3 x^2 / 2y
-        fe xx = fq::sqr(p.x);
+        fe xx = fq::sqr_fused(p.x);
         num = fq::add(fq::dbl(xx), xx);
         x2 = p.x;
     }
     fe lam = fq::mul(num, dinv);
     aff r;
-    r.x = fq::sub(fq::sub(fq::sqr(lam), p.x), x2);
+    r.x = fq::sub(fq::sub(fq::sqr_fused(lam), p.x), x2);
     r.y = fq::sub(fq::mul(lam, fq::sub(p.x, r.x)), p.y);
     return r;
 }

@@ -20,7 +20,7 @@ __global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t
     fe r;
     switch (op) {
         case MSM_G1_TEST_FQ_MUL: r = fq::mul(x, fq::load(b + 8 * i)); break;
-        case MSM_G1_TEST_FQ_SQR: r = fq::sqr(x); break;
+        case MSM_G1_TEST_FQ_SQR: r = fq::sqr_fused(x); break;  // the fused-pair squaring
         case MSM_G1_TEST_FQ_ADD: r = fq::add(x, fq::load(b + 8 * i)); break;
         case MSM_G1_TEST_FQ_SUB: r = fq::sub(x, fq::load(b + 8 * i)); break;
         case MSM_G1_TEST_FQ_NEG: r = fq::neg(x); break;

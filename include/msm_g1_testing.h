@@ -21,7 +21,7 @@ extern "C" {
  * too?"; the inversion is the one batched affine addition amortises, PR #23736,
  * section "Goal & lever"). */
 #define MSM_G1_TEST_FQ_MUL 0 /* out = a * b           */
-#define MSM_G1_TEST_FQ_SQR 1 /* out = a * a           */
+#define MSM_G1_TEST_FQ_SQR 1 /* out = a * a (the 36-product squaring of the batched additions) */
 #define MSM_G1_TEST_FQ_ADD 2 /* out = a + b           */
 #define MSM_G1_TEST_FQ_SUB 3 /* out = a - b           */
 #define MSM_G1_TEST_FQ_NEG 4 /* out = -a              */
