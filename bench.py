@@ -3,9 +3,10 @@
 
 One step = one complete MSM (digits, sort, accumulation, bucket reduction,
 window combination) over seeded synthetic inputs already resident in HBM.
-Default workload: n = 2^16 points [r_i]G, uniform scalars, window c = 13,
-batch S = 8 (the pages' "logn=16" shape; PR #23520 "cache dx + idx in
-ba_fused_super pref_scratch", section "Measurements").  Prints one JSON line.
+Default workload: n = 2^16 points [r_i]G, uniform scalars, window c = 13
+(the pages' "logn=16" shape; PR #23520 "cache dx + idx in ba_fused_super
+pref_scratch", section "Measurements"; the pages' S = 8 is their phones'
+optimum, here the library picks the batch size).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -72,7 +73,7 @@ def parse():
     ap.add_argument("--config", default="n2p16", choices=sorted(CONFIGS))
     ap.add_argument("--c", type=int, default=0, help="override the window size")
     ap.add_argument("--batch-s", type=int, default=0,
-                    help="additions per inversion: 1..64, 0 = the library's per-launch choice (32 or 64)")
+                    help="additions per thread batch: 1..64, 0 = the library's choice (64)")
     ap.add_argument("--tpb", type=int, default=128)
     ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
@@ -366,9 +367,11 @@ def run_gpu(args, cfg):
                          "count_basis": "5 Fq muls x 264 IMAD slots (128 full limb products at 2 slots + 8 low) + 1 squaring x 208 slots (36 + 64 full products + 8 low) per addition = 1528; inversion excluded",
                          "algorithmic_imad_slots_per_launch": strict_imad,
                          "adds_per_launch": adds_l0,
-                         "inversion": "%s, one per %s additions" % (
+                         "inversion": "%s; each thread's batch of up to %s additions has one product to "
+                                      "invert, and where threads hold two or more pairs the 128 threads of a "
+                                      "block share one inversion pass (warp 0)" % (
                              "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)",
-                             args.batch_s or "S (32 or 64 per launch)"),
+                             args.batch_s or 64),
                          "accumulation_frac_all_levels": adds_total * IMAD_SLOTS_PER_ADD
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,

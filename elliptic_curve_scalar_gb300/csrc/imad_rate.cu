@@ -6,7 +6,7 @@
 // Prints mad.lo / mad.hi / carry-chained madc throughput (ops/s), the rate of
 // full limb products issued as lo/hi pairs in one carry chain (the form the
 // field multiplication uses) and as unpaired lo and hi, dependent latencies
-// (cycles), and fq::mul latency and throughput.
+// (cycles), and the latency and throughput of fq::mul and fq::sqr_fused.
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>

@@ -96,8 +96,10 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)units + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t u0 = ubeg + t * chunk;
-    if (t * chunk >= units) return;
-    const int count = (int)min(chunk, (uint64_t)units - t * chunk);
+    // the block may share one inversion: a block with work keeps all its threads
+    if ((uint64_t)blockIdx.x * blockDim.x * chunk >= units) return;
+    const int count = t * chunk < units ? (int)min(chunk, (uint64_t)units - t * chunk) : 0;
+    __shared__ uint32_t sh[8 * 256];
     Level0Src<S> src;
     src.points = points;
     src.phi = phi;
@@ -109,8 +111,12 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
         src.e0[k] = e.x;
         src.e1[k] = e.y;
     }
-    int adds = batch_pairs<S, WIDE>(src, count, inv_kind);
-    if (stats) warp_stats(ctl, adds, 1);
+    // narrow launches (one pair per thread) keep per-thread inversions: the
+    // block's shared one would add warp 0's group products to their latency
+    const bool share = chunk >= 2;
+    if (!share && count == 0) return;
+    int adds = batch_pairs<S, WIDE>(src, count, inv_kind, share ? sh : nullptr);
+    if (stats) warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
 }
 
 template <int S>
@@ -222,15 +228,19 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t i0 = t * chunk;
-    if (i0 >= cnt) return;
-    const int count = (int)min(chunk, (uint64_t)cnt - i0);
+    // the block may share one inversion: a block with work keeps all its threads
+    if ((uint64_t)blockIdx.x * blockDim.x * chunk >= cnt) return;
+    const int count = i0 < cnt ? (int)min(chunk, (uint64_t)cnt - i0) : 0;
+    __shared__ uint32_t sh[8 * 256];
     ListSrc<S> src;
     src.items = items;
     src.half = 1u << (level - 1);
     for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
-    int adds = batch_pairs<S, WIDE>(src, count, inv_kind);
+    const bool share = chunk >= 2;  // as in accum_level0
+    if (!share && count == 0) return;
+    int adds = batch_pairs<S, WIDE>(src, count, inv_kind, share ? sh : nullptr);
     if (stats) {
-        warp_stats(ctl, adds, 1);
+        warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
     }
 }
@@ -272,23 +282,34 @@ void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, 
 // ----------------------------------------------------------------- launchers
 
 static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
-    // enough threads for chunks of S, but at least one resident wave when the
-    // level may hold that much work
-    uint64_t threads = std::max((work + S - 1) / S, std::min(work, resident));
+    // Chunks of S, except that a launch of fewer than four resident waves
+    // takes whole waves, the units spread evenly over them (the kernels take
+    // chunks of ceil(units / threads)): 2.25 waves of full chunks would leave
+    // the last wave three quarters empty while it still pays a whole batch's
+    // latency (n = 2^20, level 0: 1.40 -> 1.35 ms).  From four waves on the
+    // blocks' staggered finish already hides the partial wave, and the
+    // rounding only adds inversions (n = 2^22, level 0: 4.95 -> 5.01 ms).
+    // Below one wave of single units, one thread per unit.
+    uint64_t threads = work;
+    if (work > resident) {
+        const uint64_t per_wave = (uint64_t)S * resident;
+        threads = work >= 4 * per_wave ? (work + S - 1) / S : (work + per_wave - 1) / per_wave * resident;
+    }
     return (unsigned)std::max<uint64_t>(1, (threads + tpb - 1) / tpb);
 }
 
 // the register-capped build once the work fills a resident wave of the other
-static bool wide(uint64_t work, int S, const Resident& res) { return (work + S - 1) / S >= res.narrow; }
-
-// batch_s = 0 (automatic): batches of 64 once they fill two resident waves of
-// the capped build -- half the inversions per addition of 32 (n = 2^22:
-// 12.59 -> 12.24 ms) -- else 32, which keeps the last wave of a launch of
-// one or two waves from running nearly empty (n = 2^20 was 1 % slower at 64)
-static int auto_batch(int batch_s, uint64_t work, const Resident& res) {
-    if (batch_s) return batch_s;
-    return (work + 63) / 64 >= 2 * res.wide ? 64 : 32;
+// in chunks of min(S, 32)
+static bool wide(uint64_t work, int S, const Resident& res) {
+    const uint64_t s = (uint64_t)std::min(S, 32);
+    return (work + s - 1) / s >= res.narrow;
 }
+
+// batch_s = 0 (automatic): at most 64 additions per inversion.  With whole
+// waves for small launches, a larger cap never adds a wave; it only halves the
+// inversions of the launches that have more than 32 units per resident thread
+// (a cap of 32 was 4 % slower at n = 2^20 and 6 % at 2^22).
+static int auto_batch(int batch_s, uint64_t, const Resident&) { return batch_s ? batch_s : 64; }
 
 template <int S>
 static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,

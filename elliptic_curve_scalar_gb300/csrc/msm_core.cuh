@@ -192,6 +192,58 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
     return r;
 }
 
+// One inversion per block instead of one per warp.  Every thread of the block
+// brings one nonzero value a (its batch's product; 1 when it has no batch)
+// and receives a^-1.  Warp 0 gathers the block's values through shared memory
+// (sh: 8 x blockDim.x words, word w of value i at sh[w * blockDim.x + i], so
+// that consecutive lanes hit consecutive banks), lane j taking the g =
+// blockDim.x / 32 values j, j + 32, ...; it runs Montgomery's trick over its
+// g values, inverts the 32 group products in one pass of the per-lane
+// inversion, and writes the inverses back.  The other warps wait at the
+// barrier: the block issues one warp's inversion where each warp used to issue
+// its own, which at small batches (a launch of one wave, 9 additions per
+// thread at n = 2^16) is a quarter of the instructions that dominate
+// (divsteps on the ALU pipe, their 64-bit updates on the multiply pipe).
+// All threads of the block must call it; blockDim.x is a multiple of 32 and
+// at most 256.
+__device__ __forceinline__ void sh_store(uint32_t* sh, int i, const fe& a) {
+#pragma unroll
+    for (int w = 0; w < 8; w++) sh[w * blockDim.x + i] = a.v[w];
+}
+__device__ __forceinline__ fe sh_load(const uint32_t* sh, int i) {
+    fe a;
+#pragma unroll
+    for (int w = 0; w < 8; w++) a.v[w] = sh[w * blockDim.x + i];
+    return a;
+}
+
+__device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_kind) {
+    const int tid = threadIdx.x;
+    sh_store(sh, tid, a);
+    __syncthreads();
+    if (tid < 32) {
+        const int g = blockDim.x >> 5;
+        fe pre[8];
+        fe acc = sh_load(sh, tid);
+        pre[0] = acc;
+#pragma unroll 1
+        for (int i = 1; i < g; i++) {
+            acc = fq::mul(acc, sh_load(sh, tid + 32 * i));
+            pre[i] = acc;
+        }
+        fe inv = inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
+#pragma unroll 1
+        for (int i = g - 1; i > 0; i--) {
+            const fe v = sh_load(sh, tid + 32 * i);
+            sh_store(sh, tid + 32 * i, fq::mul(inv, pre[i - 1]));
+            inv = fq::mul(inv, v);
+        }
+        sh_store(sh, tid, inv);
+    }
+    __syncthreads();
+    return sh_load(sh, tid);
+}
+
 // Run one batch of up to S pair additions.  Src supplies, per slot k < count:
 //   bool has_q(k); fe xp(k), xq(k); void ys(k, fe& yp, fe& yq);
 //   aff p(k), q(k); void store(k, const aff&).
@@ -210,8 +262,11 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
 // -> 1.30 ms) through the larger loop body; inlining all six was slower still.
 // inv_kind selects the batch inversion: 0 = safegcd divsteps (the default),
 // 1 = Fermat (a^(p-2), 4-bit windows) -- kept for the measured comparison.
+// With sh (shared scratch of 8 x blockDim.x words) the block's threads share
+// one inversion (block_inverse): then every thread of the block must call,
+// those without pairs with count = 0.
 template <int S, bool INLINE_BACK, class Src>
-__device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0) {
+__device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0, uint32_t* sh = nullptr) {
     fe pre[S];
     fe acc = fq::one();
     int adds = 0;
@@ -227,7 +282,7 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
         acc = (k == 0) ? d : fq::mul_inline(acc, d);
         pre[k] = acc;
     }
-    fe inv = inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
+    fe inv = sh ? block_inverse(acc, sh, inv_kind) : inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
 #pragma unroll 1
     for (int k = count - 1; k >= 0; k--) {
         aff p = src.p(k);

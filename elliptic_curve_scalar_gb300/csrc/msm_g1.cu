@@ -939,7 +939,10 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     // Serial schedule (one stream, one window group) when phase timing is on --
     // the phase events then delimit whole phases -- or when the context has no
     // streams of its own; otherwise window groups are pipelined (below).
-    const int groups = c->groups ? c->groups : 2;  // two groups measured best (n = 2^16 .. 2^22)
+    // two groups for small MSMs, three from 2^19 points (GB300: n = 2^20 4.10 ->
+    // 4.00 ms, 2^22 12.13 -> 12.07 ms; at 2^16 three were 3 % slower, four
+    // slower everywhere)
+    const int groups = c->groups ? c->groups : (n >= ((size_t)1 << 19) ? 3 : 2);
     const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1 && count == 1;
     uint64_t pairs_total = 0;
     // (a batch's windows hold only their own MSM's terms: ceil(terms / count)

@@ -71,14 +71,17 @@ struct PairArraySrc {
     __device__ __forceinline__ void store(int k, const aff& r) { g1::store_aff(out + 16 * (i0 + k), r); }
 };
 
+// block: the block's threads share one inversion (all of them call, those
+// past the end with no pairs), as in the accumulation kernels
 template <int S, bool INLINE_BACK>
-__global__ void k_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+__global__ void k_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n, int block) {
+    __shared__ uint32_t sh[8 * 256];
     size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     size_t i0 = t * S;
-    if (i0 >= n) return;
-    int count = (int)((n - i0) < (size_t)S ? (n - i0) : (size_t)S);
+    if (block ? (size_t)blockIdx.x * blockDim.x * S >= n : i0 >= n) return;
+    int count = i0 >= n ? 0 : (int)((n - i0) < (size_t)S ? (n - i0) : (size_t)S);
     PairArraySrc<S> src{a, b, out, i0};
-    msm::batch_pairs<S, INLINE_BACK>(src, count);
+    msm::batch_pairs<S, INLINE_BACK>(src, count, 0, block ? sh : nullptr);
 }
 
 __global__ void k_test_digits(const uint32_t* scalars, size_t n, int c, int nbits, int32_t* digits) {
@@ -135,18 +138,20 @@ extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint
 }
 
 extern "C" int msm_g1_test_batch_add(const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n, int batch_s,
-                                     int inline_back, cudaStream_t st) {
+                                     int mode, cudaStream_t st) {
     if (n == 0) return MSM_G1_OK;
-    if (!a || !b || !out || !a16(a) || !a16(b) || !a16(out)) return MSM_G1_ERR_INVALID_ARG;
+    if (!a || !b || !out || !a16(a) || !a16(b) || !a16(out) || mode < 0 || mode > 3) return MSM_G1_ERR_INVALID_ARG;
+    const bool inline_back = mode & 1;
+    const int block = (mode >> 1) & 1;
     size_t threads;
     switch (batch_s) {
 #define CASE(S)                                                                                  \
     case S:                                                                                      \
         threads = (n + S - 1) / S;                                                               \
         if (inline_back)                                                                         \
-            k_test_batch_add<S, true><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n); \
+            k_test_batch_add<S, true><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n, block); \
         else                                                                                     \
-            k_test_batch_add<S, false><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n); \
+            k_test_batch_add<S, false><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(a, b, out, n, block); \
         break;
         CASE(1) CASE(2) CASE(4) CASE(8) CASE(16) CASE(32) CASE(64)
 #undef CASE

@@ -309,11 +309,12 @@ def test_g1(op, a, b=None, stream=None):
     return out
 
 
-def test_batch_add(a, b, batch_s, inline_back=0, stream=None):
+def test_batch_add(a, b, batch_s, inline_back=0, block=0, stream=None):
     n = a.shape[0]
     out = torch.empty_like(a)
+    mode = (1 if inline_back else 0) | (2 if block else 0)
     _check(lib().msm_g1_test_batch_add(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
-                                       ctypes.c_void_p(out.data_ptr()), n, batch_s, inline_back,
+                                       ctypes.c_void_p(out.data_ptr()), n, batch_s, mode,
                                        _stream_handle(stream)),
            "msm_g1_test_batch_add")
     return out

@@ -44,11 +44,14 @@ int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 /* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i
  * for affine a, b (16 uint32 each), with one field inversion shared by each
  * run of batch_s consecutive pairs (batch_s as MSM_G1_PARAM_BATCH_S).
- * Equal, opposite and infinite operands are allowed.  inline_back selects the
+ * Equal, opposite and infinite operands are allowed.  mode bit 0 selects the
  * build the large accumulation launches use (the backward multiplications of
- * the batch inlined, 1) or the one of small launches (called, 0). */
+ * the batch inlined, 1) or the one of small launches (called, 0); bit 1 makes
+ * the 128 threads of each block share one inversion as the accumulation
+ * kernels do (2) instead of one inversion per thread (0).  Other mode values
+ * are INVALID_ARG. */
 int msm_g1_test_batch_add(const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, int batch_s,
-                          int inline_back, cudaStream_t stream);
+                          int mode, cudaStream_t stream);
 
 /* Signed window digits of n scalars (8 uint32 each) as the MSM forms them:
  * digits (n x W int32, W = ceil(nbits/c), window-major per scalar), nbits =

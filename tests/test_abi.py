@@ -90,6 +90,7 @@ def test_argument_checks_before_device_work(lib):
     assert lib.msm_g1_mul_generator(None, None, 0, None, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_test_fq(99, None, None, None, 1, None) == gm.ERR_INVALID_ARG
     assert lib.msm_g1_test_batch_add(vp(16), vp(16), vp(16), 4, 3, 0, None) == gm.ERR_INVALID_ARG
+    assert lib.msm_g1_test_batch_add(vp(16), vp(16), vp(16), 4, 4, 4, None) == gm.ERR_INVALID_ARG
     lib.msm_g1_destroy(None)
 
 

@@ -84,11 +84,14 @@ def test_jacobian_ops():
         assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
 
 
+@pytest.mark.parametrize("block", [0, 1])
 @pytest.mark.parametrize("inline_back", [0, 1])
 @pytest.mark.parametrize("batch_s", [1, 2, 4, 8, 16, 32, 64])
-def test_batch_affine_add(batch_s, inline_back):
+def test_batch_affine_add(batch_s, inline_back, block):
     """Batched affine pair additions, including pairs that would poison a
-    shared inversion: equal points (tangent), opposite points, infinity."""
+    shared inversion: equal points (tangent), opposite points, infinity;
+    per-thread inversions and one inversion shared by the block's threads
+    (whose tail threads have no pairs)."""
     rng = random.Random(100 + batch_s)
     pts = _rand_points(rng, 60)
     a, b = [], []
@@ -107,7 +110,7 @@ def test_batch_affine_add(batch_s, inline_back):
         b.append(q)
     da = gm.to_device(np.stack([point_to_aff_words(p) for p in a]))
     db = gm.to_device(np.stack([point_to_aff_words(p) for p in b]))
-    out = gm.to_host(gm.test_batch_add(da, db, batch_s, inline_back))
+    out = gm.to_host(gm.test_batch_add(da, db, batch_s, inline_back, block))
     for i, (p, q) in enumerate(zip(a, b)):
         assert aff_words_to_point(out[i]) == pyref.add(p, q), (batch_s, i)
 
