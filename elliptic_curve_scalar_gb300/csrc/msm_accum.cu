@@ -25,6 +25,7 @@
 
 #include <algorithm>
 
+#include "g1_coop.cuh"
 #include "msm_internal.cuh"
 
 using fq::fe;
@@ -115,7 +116,9 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     // block's shared one would add warp 0's group products to their latency
     const bool share = chunk >= 2;
     if (!share && count == 0) return;
-    int adds = batch_pairs<S, WIDE>(src, count, inv_kind, share ? sh : nullptr);
+    // the backward multiplications inlined in both builds of level 0 (n = 2^16,
+    // natural build: 131 -> 127 us); the tree's narrow levels keep them called
+    int adds = batch_pairs<S, true>(src, count, inv_kind, share ? sh : nullptr);
     if (stats) warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
 }
 
@@ -258,25 +261,33 @@ __global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, 
 
 // ------------------------------------------------------------ small buckets
 
-// One thread per bucket: buckets that left the tree with 2..T items get their
-// sum by Jacobian mixed additions (see finish_plan in msm_core.cuh).
+// One thread (W = 1) or one group of W lanes (cooperative additions) per bucket:
+// buckets that left the tree with 2..T items get their sum by Jacobian mixed
+// additions (see finish_plan in msm_core.cuh).
+template <int W>
 __global__ void k_finish(const uint32_t* __restrict__ items, const uint32_t* __restrict__ offsets, uint32_t g0,
                          uint32_t g1, uint32_t finish_t, uint32_t* __restrict__ jsum) {
-    const uint32_t g = g0 + blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t g = g0 + (blockIdx.x * blockDim.x + threadIdx.x) / W;
     if (g >= g1) return;
     const uint32_t og = offsets[g] >> 1;
     const uint32_t h = (offsets[g + 1] >> 1) - og;
     const FinishPlan fp = finish_plan(h, finish_t);
     if (fp.items < 2) return;
     g1::jac acc = g1::jac_inf();
-    for (uint32_t i = 0; i < fp.items; i++) acc = g1::add_mixed(acc, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
-    g1::store_jac(jsum + (size_t)g * 24, acc);
+    for (uint32_t i = 0; i < fp.items; i++)
+        acc = g1c::add_mixed_w<W>(acc, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
+    if ((threadIdx.x & (W - 1)) == 0) g1::store_jac(jsum + (size_t)g * 24, acc);
 }
 
 void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,
-                   uint32_t* jsum, cudaStream_t st) {
+                   uint32_t* jsum, uint64_t resident, cudaStream_t st) {
     if (finish_t < 2 || g1 <= g0) return;
-    k_finish<<<(g1 - g0 + 127) / 128, 128, 0, st>>>(items, offsets, g0, g1, finish_t, jsum);
+    // cooperative groups of 8 lanes while the buckets fill a quarter of the GPU
+    // at most (the chunk reduction's rule)
+    if ((uint64_t)(g1 - g0) * 8 <= resident / 4)
+        k_finish<8><<<((g1 - g0) * 8 + 127) / 128, 128, 0, st>>>(items, offsets, g0, g1, finish_t, jsum);
+    else
+        k_finish<1><<<(g1 - g0 + 127) / 128, 128, 0, st>>>(items, offsets, g0, g1, finish_t, jsum);
 }
 
 // ----------------------------------------------------------------- launchers

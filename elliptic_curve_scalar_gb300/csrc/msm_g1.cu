@@ -254,6 +254,133 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
     });
 }
 
+// ------------------------------------------ 3'. sort of large single MSMs
+//
+// With 2^23 terms and 8 windows the two passes above issue 67 M global atomics
+// each, and the scalar split runs twice.  For large single MSMs (window width
+// at most 16, so a window's B counters fit in shared memory) the digits are
+// formed once into a code matrix, and every block counts one slice of one
+// window's codes in shared memory: one global atomic per bucket and block
+// instead of one per digit, and the scatter writes one window's region of
+// the entry list at a time, which stays in L2.  The order of the entries
+// within a bucket is whatever the shared atomics give: a bucket's sum does
+// not depend on it.
+
+// code of one (term, window): NO_DIGIT for digit 0, else (|d| - 1) | negate << 31.
+// (32-bit codes: with 16-bit windows the 2^15 buckets and the sign fill 16
+// bits, and no 16-bit value would be left for "no digit".)
+constexpr uint32_t NO_DIGIT = 0xFFFFFFFFu;
+
+// One thread per scalar: its W codes per half, codes[w * tstride + t] for term t
+// (t = i, and n + i for the GLV half on phi(P_i)).
+template <bool GLV>
+__global__ void k_digit_codes(const uint32_t* __restrict__ scalars, size_t n, Windows L, size_t tstride,
+                              uint32_t* __restrict__ codes) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    uint32_t k[8];
+    load_scalar(scalars + 8 * i, k);
+    reduce_mod_r(k);
+    auto emit = [&](auto& half, size_t t, uint32_t neg) {
+        uint32_t carry = 0;
+        for (int w = 0; w < L.W; w++) {
+            const int d = signed_digit(half, L, w, carry);
+            const uint32_t mag = (uint32_t)(d < 0 ? -d : d);
+            codes[(size_t)w * tstride + t] = d == 0 ? NO_DIGIT : (mag - 1u) | ((((uint32_t)(d < 0)) ^ neg) << 31);
+        }
+    };
+    if constexpr (GLV) {
+        uint32_t k1[4], k2[4], neg1, neg2;
+        glv::split(k, k1, k2, neg1, neg2);
+        emit(k1, i, neg1);
+        emit(k2, n + i, neg2);
+    } else {
+        emit(k, i, 0u);
+    }
+}
+
+// Block b: window b / S, terms [s T, min((s + 1) T, nterms)) with s = b % S and
+// T a multiple of 4 (codes read 4 at a time; the row stride is a multiple of 4
+// and its padding is read but ignored).  sh: B shared counters.
+__device__ __forceinline__ void slice_counts(const uint32_t* __restrict__ row, size_t t0, size_t t1, uint32_t* sh) {
+    for (size_t t = t0 + 4 * (size_t)threadIdx.x; t < t1; t += 4 * (size_t)blockDim.x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
+        const uint32_t cd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (cd[j] != NO_DIGIT && t + j < t1) atomicAdd(&sh[cd[j] & ~SIGN], 1u);
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_hist_slices(const uint32_t* __restrict__ codes, size_t tstride,
+                                                      size_t nterms, uint32_t S, size_t T, uint32_t B,
+                                                      uint32_t* __restrict__ counts) {
+    extern __shared__ uint32_t sh[];
+    const uint32_t w = blockIdx.x / S, s = blockIdx.x % S;
+    const size_t t0 = (size_t)s * T, t1 = min(t0 + T, nterms);
+    for (uint32_t b = threadIdx.x; b < B; b += blockDim.x) sh[b] = 0;
+    __syncthreads();
+    if (t0 < t1) slice_counts(codes + (size_t)w * tstride, t0, t1, sh);
+    __syncthreads();
+    for (uint32_t b = threadIdx.x; b < B; b += blockDim.x)
+        if (sh[b]) atomicAdd(&counts[(size_t)w * B + b], sh[b]);
+}
+
+// The same slices again: count, reserve each bucket's run in the entry list
+// with one global atomic on its cursor, then place every entry at the
+// reservation's next free slot (a shared atomic).
+__global__ void __launch_bounds__(1024) k_scatter_slices(const uint32_t* __restrict__ codes, size_t tstride,
+                                                         size_t nterms, uint32_t S, size_t T, uint32_t B,
+                                                         uint32_t* __restrict__ cursor,
+                                                         uint32_t* __restrict__ entries) {
+    extern __shared__ uint32_t sh[];
+    const uint32_t w = blockIdx.x / S, s = blockIdx.x % S;
+    const size_t t0 = (size_t)s * T, t1 = min(t0 + T, nterms);
+    const uint32_t* row = codes + (size_t)w * tstride;
+    for (uint32_t b = threadIdx.x; b < B; b += blockDim.x) sh[b] = 0;
+    __syncthreads();
+    if (t0 < t1) slice_counts(row, t0, t1, sh);
+    __syncthreads();
+    for (uint32_t b = threadIdx.x; b < B; b += blockDim.x)
+        if (sh[b]) sh[b] = atomicAdd(&cursor[(size_t)w * B + b], sh[b]);
+    __syncthreads();
+    for (size_t t = t0 + 4 * (size_t)threadIdx.x; t < t1; t += 4 * (size_t)blockDim.x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
+        const uint32_t cd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (cd[j] != NO_DIGIT && t + j < t1) {
+                const uint32_t pos = atomicAdd(&sh[cd[j] & ~SIGN], 1u);
+                entries[pos] = (uint32_t)(t + j) | (cd[j] & SIGN);
+            }
+        }
+    }
+}
+
+// The scatter of the codes in term order, one thread per term and window row,
+// the lanes of a warp that hit the same bucket sharing one atomic (like
+// k_scatter, without recomputing the digits).  Every bucket then fills from
+// its start in term order: one partial sector per bucket is being written at
+// any time, which L2 holds even when the entry list does not fit (n = 2^22:
+// 268 MB of entries; the slices' per-block runs, 152 write fronts per bucket,
+// thrashed L2: 0.75 -> 2.0 ms).
+__global__ void k_scatter_codes(const uint32_t* __restrict__ codes, size_t tstride, size_t nterms, int W,
+                                uint32_t B, uint32_t* __restrict__ cursor, uint32_t* __restrict__ entries) {
+    const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int w = 0; w < W; w++) {
+        const uint32_t cd = t < nterms ? codes[(size_t)w * tstride + t] : NO_DIGIT;
+        const uint32_t g = cd == NO_DIGIT ? HOLE : (uint32_t)w * B + (cd & ~SIGN);
+        const uint32_t peers = __match_any_sync(0xffffffffu, g);
+        const int leader = __ffs(peers) - 1;
+        uint32_t pos = 0;
+        if (g != HOLE && lane == leader) pos = atomicAdd(&cursor[g], (uint32_t)__popc(peers));
+        pos = __shfl_sync(0xffffffffu, pos, leader);
+        if (g != HOLE) entries[pos + __popc(peers & lt_mask)] = (uint32_t)t | (cd & SIGN);
+    }
+}
+
 // ---------------------------------------------------------- 6. reduction
 //
 // T_w = sum_{b<B} (b + 1) S_b per window, without a per-chunk scalar multiple.
@@ -267,11 +394,15 @@ __global__ void k_scatter(const uint32_t* __restrict__ scalars, size_t n, int c,
 
 // One thread per chunk: running sums from the chunk's top bucket give
 // run = R_j and sum = C_j (bucket jL + i is added into run at steps i .. 0).
+template <int W>
 __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ counts,
                                 const uint32_t* __restrict__ offsets, const uint32_t* __restrict__ jsum,
                                 uint32_t finish_t, int w_lo, int nwin, uint32_t B, uint32_t L, uint32_t G,
                                 uint32_t* __restrict__ chunks) {
-    uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    // one thread (W = 1) or one group of W lanes per chunk, whose additions
+    // are then cooperative: 5 multiplication latencies each instead of 11 or
+    // 16, for 2.5 times the multiply-pipe work (idle lanes multiply too)
+    uint32_t t = (blockIdx.x * blockDim.x + threadIdx.x) / W;
     if (t >= (uint32_t)nwin * G) return;
     uint32_t w = (uint32_t)w_lo + t / G, j = t % G;
     uint32_t b0 = j * L;
@@ -282,15 +413,17 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
         if (counts[g]) {
             const uint32_t og = offsets[g] >> 1;
             if (finish_plan((offsets[g + 1] >> 1) - og, finish_t).items >= 2)
-                run = g1::add(run, g1::load_jac(jsum + (size_t)g * 24));  // finished in Jacobian
+                run = g1c::add_w<W>(run, g1::load_jac(jsum + (size_t)g * 24));  // finished in Jacobian
             else
-                run = g1::add_mixed(run, g1::load_aff(items + (size_t)og * 16));
+                run = g1c::add_mixed_w<W>(run, g1::load_aff(items + (size_t)og * 16));
         }
-        sum = g1::add(sum, run);
+        sum = g1c::add_w<W>(sum, run);
     }
-    uint32_t* dst = chunks + ((size_t)w * G + j) * 48;
-    g1::store_jac(dst, sum);
-    g1::store_jac(dst + 24, run);
+    if ((threadIdx.x & (W - 1)) == 0) {
+        uint32_t* dst = chunks + ((size_t)w * G + j) * 48;
+        g1::store_jac(dst, sum);
+        g1::store_jac(dst + 24, run);
+    }
 }
 
 // Sum of the n Jacobian points in sm[0 .. n) (n a power of two, n <= blockDim.x
@@ -401,6 +534,26 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
 }
 
+// In the pipelined schedule a later group's windows w_lo .. w_hi-1 enter the
+// running value Q as Q' = 2^(off_hi - off_lo) Q + L, where L is the group's
+// own Horner value (k_combine_part with first = 1, on the group's stream).
+// The shift depends on the earlier groups only, so it runs while the group is
+// still accumulating, and the group's sums leave only L's shorter chain and
+// one addition on the critical path.
+__global__ void k_combine_shift(uint32_t* __restrict__ acc, int bits) {
+    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
+    jac q = g1::load_jac(acc);
+    for (int i = 0; i < bits; i++) q = g1c::dbl(q);
+    if (threadIdx.x == 0) g1::store_jac(acc, q);
+}
+
+__global__ void k_combine_join(uint32_t* __restrict__ acc, const uint32_t* __restrict__ loc,
+                               uint32_t* __restrict__ out, int last) {
+    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
+    jac q = g1c::add(g1::load_jac(acc), g1::load_jac(loc));
+    if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
+}
+
 // Batches: one warp per MSM m, Horner's rule over its windows [m W, (m + 1) W).
 __global__ void k_combine_batch(const uint32_t* __restrict__ wsums, Windows L, uint32_t* __restrict__ out) {
     const uint32_t m = blockIdx.x;
@@ -471,7 +624,7 @@ struct msm_g1_ctx {
     uint32_t* msm_off;     // term offsets of the MSMs of a batch (device)
     uint64_t cap_windows, cap_partials;
     uint32_t* pairs;
-    uint32_t* qacc;        // running value of the window combination between groups
+    uint32_t* qacc;        // running value of the window combination, then one value per window group
     uint32_t* jsum;        // Jacobian bucket sums of buckets finished outside the tree
     uint32_t* phi;         // phi(P_i) = (beta x_i, y_i) for the GLV split
     int glv;               // 1: split scalars by the endomorphism (default)
@@ -480,6 +633,8 @@ struct msm_g1_ctx {
     Resident resident[3];  // resident accumulation threads for tpb = 64, 128, 256
     int groups;            // window groups of the pipelined schedule (1 = serial)
     bool streams_ok;       // the context's own streams and events exist
+    bool slice_sort_ok;    // the shared-memory sort kernels may take 128 KB of shared memory
+    int sms;               // streaming multiprocessors of the device
     cudaStream_t acc_stream[MAX_GROUPS], chain_stream;
     cudaEvent_t ev_fork, ev_group[MAX_GROUPS], ev_chain;
     cudaStream_t side_stream;    // points upload and phi beside the sort
@@ -651,7 +806,7 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
     size_t o_table = take((size_t)64 * 256);
     size_t o_tj = take((size_t)96 * 256);
     size_t o_pairs = take((size_t)4 * s.pairs);
-    size_t o_qacc = take((size_t)96);
+    size_t o_qacc = take((size_t)96 * (1 + MAX_GROUPS));  // running value, one local value per group
     size_t o_jsum = take((size_t)96 * s.buckets);
     size_t o_phi = take((size_t)64 * s.points);
     if (assign) {
@@ -732,6 +887,7 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
     msm_g1_ctx* c = (msm_g1_ctx*)calloc(1, sizeof(msm_g1_ctx));
     if (!c) return MSM_G1_ERR_ALLOC;
     c->device = dev;
+    c->sms = prop.multiProcessorCount;
     c->max_n = max_n;
     c->max_c = max_c;
     c->cap_entries = s.entries;
@@ -773,6 +929,11 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
             ok = ok && cudaEventCreateWithFlags(&c->ev_group[j], cudaEventDisableTiming) == cudaSuccess;
         cudaGetLastError();
         c->streams_ok = ok;  // without them every run takes the serial schedule
+        const int smem = 4 << 15;  // B = 2^15 counters, window width 16
+        c->slice_sort_ok =
+            cudaFuncSetAttribute(k_hist_slices, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+            cudaFuncSetAttribute(k_scatter_slices, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+        cudaGetLastError();
     }
     *out = c;
     return MSM_G1_OK;
@@ -925,7 +1086,21 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     }
     CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
     CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
-    {
+    // large single MSMs with windows of at most 16 bits take the shared-memory
+    // sort (digit codes once, slices of one window per block); its code matrix
+    // lives in the item buffer, which the accumulation fills only afterwards
+    const bool slice_sort = c->slice_sort_ok && count == 1 && cw <= 16 && terms * W >= ((uint64_t)1 << 22);
+    const size_t tstride = (size_t)((terms + 3) & ~(uint64_t)3);
+    uint32_t* codes = c->items;
+    const uint32_t slices = (uint32_t)std::max(1, c->sms / W);
+    const size_t slice_t = (size_t)(((terms + slices - 1) / slices + 3) & ~(uint64_t)3);
+    if (slice_sort) {
+        unsigned blocks = (unsigned)((n + 255) / 256);
+        if (glv) k_digit_codes<true><<<blocks, 256, 0, st>>>(scalars, n, win, tstride, codes);
+        else k_digit_codes<false><<<blocks, 256, 0, st>>>(scalars, n, win, tstride, codes);
+        k_hist_slices<<<(unsigned)W * slices, 1024, 4 * B, st>>>(codes, tstride, terms, slices, slice_t, B, c->counts);
+        launches += 2;
+    } else {
         unsigned blocks = (unsigned)((n + 255) / 256);
         if (glv) k_digits_hist<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->counts);
         else k_digits_hist<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->counts);
@@ -943,6 +1118,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     // 4.00 ms, 2^22 12.13 -> 12.07 ms; at 2^16 three were 3 % slower, four
     // slower everywhere)
     const int groups = c->groups ? c->groups : (n >= ((size_t)1 << 19) ? 3 : 2);
+    const bool split_combine = n < ((size_t)1 << 19);
     const bool pipelined = c->streams_ok && !c->timing && groups > 1 && W > 1 && count == 1;
     uint64_t pairs_total = 0;
     // (a batch's windows hold only their own MSM's terms: ceil(terms / count)
@@ -954,7 +1130,16 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
     mark(2);
-    {
+    if (slice_sort) {
+        // per-slice runs while the entry list fits in L2, else term order
+        if (terms * W * 4 <= ((uint64_t)64 << 20))
+            k_scatter_slices<<<(unsigned)W * slices, 1024, 4 * B, st>>>(codes, tstride, terms, slices, slice_t, B,
+                                                                        c->cursor, c->entries);
+        else
+            k_scatter_codes<<<(unsigned)((terms + 255) / 256), 256, 0, st>>>(codes, tstride, terms, W, B, c->cursor,
+                                                                             c->entries);
+        launches++;
+    } else {
         unsigned blocks = (unsigned)((n + 255) / 256);
         if (glv) k_scatter<true><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->cursor, c->entries);
         else k_scatter<false><<<blocks, 256, 0, st>>>(scalars, n, cw, win, bm, c->cursor, c->entries);
@@ -992,11 +1177,18 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         const uint32_t threads = (uint32_t)nw * G;
         if (lay.finish_t >= 2) {
             launch_finish(c->items, c->offsets, (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, lay.finish_t,
-                          c->jsum, s);
+                          c->jsum, c->resident[1].narrow, s);
             launches++;
         }
-        k_reduce_chunks<<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum, lay.finish_t,
-                                                             lay.w_lo[j], nw, B, L, G, c->chunks);
+        // cooperative groups while the chunks fill a quarter of the GPU at most
+        // (n = 2^10, 512 chunks: reduction 0.22 -> 0.18 ms; at 2^16, with 5 k
+        // chunks per group, they made the MSM 2 % slower: idle lanes multiply)
+        if ((uint64_t)threads * 8 <= c->resident[1].narrow / 4)
+            k_reduce_chunks<8><<<(threads * 8 + 127) / 128, 128, 0, s>>>(
+                c->items, c->counts, c->offsets, c->jsum, lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
+        else
+            k_reduce_chunks<1><<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum,
+                                                                    lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
         k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, rp.tpb, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
                                                                           rp.parts, rp.m, c->partials);
         k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L), c->wsums);
@@ -1033,9 +1225,26 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
             level0(j, s);
             tree(j, s);
             reduce(j, s);
+            // below 2^19 points the later groups' combination is split (n = 2^10:
+            // 0.714 -> 0.675 ms, 2^16: 1.071 -> 1.048 ms); for larger MSMs, with
+            // three groups, the group's own Horner chain on its low-priority
+            // stream waited behind the accumulation (2^20: 3.84 -> 3.91 ms)
+            if (j == 0 || !split_combine) {
+                CK(cudaEventRecord(c->ev_group[j], s));
+                CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
+                combine(j, c->chain_stream);
+                continue;
+            }
+            // the group's own Horner value on its stream; on the chain, the
+            // running value shifted past the group's windows, then the join
+            uint32_t* loc = c->qacc + 24 * (1 + j);
+            k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, loc, out, 1, 0);
             CK(cudaEventRecord(c->ev_group[j], s));
+            k_combine_shift<<<1, 32, 0, c->chain_stream>>>(
+                c->qacc, window_offset(win, lay.w_hi[j]) - window_offset(win, lay.w_lo[j]));
             CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
-            combine(j, c->chain_stream);
+            k_combine_join<<<1, 32, 0, c->chain_stream>>>(c->qacc, loc, out, j == lay.groups - 1);
+            launches += 3;
         }
         CK(cudaEventRecord(c->ev_chain, c->chain_stream));
         CK(cudaStreamWaitEvent(st, c->ev_chain, 0));

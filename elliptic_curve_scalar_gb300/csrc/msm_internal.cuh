@@ -60,6 +60,6 @@ void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* ite
 Resident accum_resident_threads(int tpb);
 // Jacobian sums of the buckets of [g0, g1) that left the tree with >= 2 items
 void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,
-                   uint32_t* jsum, cudaStream_t st);
+                   uint32_t* jsum, uint64_t resident, cudaStream_t st);
 
 }  // namespace msm

@@ -45,13 +45,21 @@ __global__ void k_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t
     }
 }
 
-// one warp per element, all lanes holding the same operands
+// one group of W lanes per element (W = 32: a warp; W = 8: four elements per
+// warp, whose groups may take different branches), all lanes of a group
+// holding the same operands
+template <int W>
 __global__ void k_test_g1_coop(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
-    size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) / W;
     if (i >= n) return;
-    jac r = op == MSM_G1_TEST_JAC_DBL_COOP ? g1c::dbl(g1::load_jac(a + 24 * i))
-                                           : g1c::add(g1::load_jac(a + 24 * i), g1::load_jac(b + 24 * i));
-    if ((threadIdx.x & 31) == 0) g1::store_jac(out + 24 * i, r);
+    jac r;
+    if (op == MSM_G1_TEST_JAC_DBL_COOP || op == MSM_G1_TEST_JAC_DBL_COOP8)
+        r = g1c::dbl<W>(g1::load_jac(a + 24 * i));
+    else if (op == MSM_G1_TEST_JAC_ADD_COOP || op == MSM_G1_TEST_JAC_ADD_COOP8)
+        r = g1c::add<W>(g1::load_jac(a + 24 * i), g1::load_jac(b + 24 * i));
+    else
+        r = g1c::add_mixed<W>(g1::load_jac(a + 24 * i), g1::load_aff(b + 16 * i));
+    if ((threadIdx.x & (W - 1)) == 0) g1::store_jac(out + 24 * i, r);
 }
 
 template <int S>
@@ -126,12 +134,15 @@ extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint
 
 extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_ADD_COOP) return MSM_G1_ERR_INVALID_ARG;
-    bool needs_b = op == MSM_G1_TEST_JAC_ADD || op == MSM_G1_TEST_JAC_MIXED || op == MSM_G1_TEST_JAC_ADD_COOP;
+    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_MIXED_COOP8) return MSM_G1_ERR_INVALID_ARG;
+    bool needs_b = op != MSM_G1_TEST_JAC_DBL && op != MSM_G1_TEST_TO_AFFINE && op != MSM_G1_TEST_JAC_DBL_COOP &&
+                   op != MSM_G1_TEST_JAC_DBL_COOP8;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
-    if (op >= MSM_G1_TEST_JAC_DBL_COOP)
-        k_test_g1_coop<<<(unsigned)((n * 32 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    if (op >= MSM_G1_TEST_JAC_DBL_COOP8)
+        k_test_g1_coop<8><<<(unsigned)((n * 8 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
+    else if (op >= MSM_G1_TEST_JAC_DBL_COOP)
+        k_test_g1_coop<32><<<(unsigned)((n * 32 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
     else
         k_test_g1<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
     return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;

@@ -31,14 +31,20 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 
 /* Point operations.  JAC_* take and return Jacobian points (24 uint32),
  * MIXED adds a Jacobian a and an affine b, TO_AFFINE normalises a Jacobian a
- * into an affine out (16 uint32).  *_COOP are the warp-cooperative doubling
- * and addition of the window combination (one warp per element). */
+ * into an affine out (16 uint32).  *_COOP are the cooperative doubling,
+ * addition and mixed addition of the window combination (one warp per
+ * element); *_COOP8 the same with one group of 8 lanes per element, as the
+ * bucket reduction runs them (four elements per warp). */
 #define MSM_G1_TEST_JAC_DBL 0
 #define MSM_G1_TEST_JAC_ADD 1
 #define MSM_G1_TEST_JAC_MIXED 2
 #define MSM_G1_TEST_TO_AFFINE 3
 #define MSM_G1_TEST_JAC_DBL_COOP 4
 #define MSM_G1_TEST_JAC_ADD_COOP 5
+#define MSM_G1_TEST_JAC_MIXED_COOP 6
+#define MSM_G1_TEST_JAC_DBL_COOP8 7
+#define MSM_G1_TEST_JAC_ADD_COOP8 8
+#define MSM_G1_TEST_JAC_MIXED_COOP8 9
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i

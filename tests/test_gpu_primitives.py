@@ -73,6 +73,12 @@ def test_jacobian_ops():
     # the same sums with the operands of the special cases swapped and with P + P
     addc2 = gm.to_host(gm.test_g1("jac_add_coop", db, da))
     addc3 = gm.to_host(gm.test_g1("jac_add_coop", da, da))
+    mixc = gm.to_host(gm.test_g1("jac_mixed_coop", da, dab))
+    # groups of 8 lanes: four elements per warp, whose special cases differ
+    dbl8 = gm.to_host(gm.test_g1("jac_dbl_coop8", da))
+    add8 = gm.to_host(gm.test_g1("jac_add_coop8", da, db))
+    add8s = gm.to_host(gm.test_g1("jac_add_coop8", db, da))
+    mix8 = gm.to_host(gm.test_g1("jac_mixed_coop8", da, dab))
     for i, (p, q) in enumerate(zip(a, b)):
         assert jac_words_to_point(dbl[i]) == pyref.add(p, p), ("dbl", i)
         assert jac_words_to_point(add[i]) == pyref.add(p, q), ("add", i)
@@ -81,6 +87,11 @@ def test_jacobian_ops():
         assert jac_words_to_point(addc2[i]) == pyref.add(q, p), ("add_coop swapped", i)
         assert jac_words_to_point(addc3[i]) == pyref.add(p, p), ("add_coop P+P", i)
         assert jac_words_to_point(mix[i]) == pyref.add(p, q), ("mixed", i)
+        assert jac_words_to_point(mixc[i]) == pyref.add(p, q), ("mixed_coop", i)
+        assert jac_words_to_point(dbl8[i]) == pyref.add(p, p), ("dbl_coop8", i)
+        assert jac_words_to_point(add8[i]) == pyref.add(p, q), ("add_coop8", i)
+        assert jac_words_to_point(add8s[i]) == pyref.add(q, p), ("add_coop8 swapped", i)
+        assert jac_words_to_point(mix8[i]) == pyref.add(p, q), ("mixed_coop8", i)
         assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
 
 
