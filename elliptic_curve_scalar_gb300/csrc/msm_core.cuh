@@ -258,8 +258,9 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
 // moves into and out of the call's argument registers (which occupy the same
 // multiply pipe the products do) and leaves the register allocator a global
 // view.  Inlining the backward pair pays for large, throughput-bound launches
-// (n = 2^22: 12.98 -> 12.79 ms) and costs latency-bound ones (n = 2^16: 1.27
-// -> 1.30 ms) through the larger loop body; inlining all six was slower still.
+// (n = 2^22: 12.98 -> 12.79 ms) and for level 0 at any size, and costs the
+// tree's latency-bound narrow levels through the larger loop body (the
+// accumulation kernels choose); inlining all six was slower still.
 // inv_kind selects the batch inversion: 0 = safegcd divsteps (the default),
 // 1 = Fermat (a^(p-2), 4-bit windows) -- kept for the measured comparison.
 // With sh (shared scratch of 8 x blockDim.x words) the block's threads share
