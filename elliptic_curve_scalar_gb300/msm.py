@@ -34,6 +34,7 @@ PARAM_GROUPS = 5
 PARAM_FINISH = 6
 PARAM_GLV = 7
 PARAM_INVERSION = 8
+PARAM_GRAPH = 9
 PLAIN_BITS = 255  # bits the signed windows of a scalar mod r cover
 GLV_BITS = 128    # bits the signed windows of one GLV half cover
 

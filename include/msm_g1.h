@@ -55,16 +55,21 @@ extern "C" {
 
 /* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
 #define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32, 64,
-                                  or 0 = per launch (default): 64 where such batches fill two resident waves, else 32 */
+                                  or 0 = automatic (default, 64) */
 #define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
-#define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = 2 (default) */
+#define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = automatic
+                                  (default: 2, and 3 from 2^19 points) */
 #define MSM_G1_PARAM_FINISH 6  /* buckets with at most T items leave the affine tree and are summed in
                                   Jacobian coordinates: T = 1..64, 1 = never, 0 = automatic (default) */
 #define MSM_G1_PARAM_GLV 7     /* 1: split every scalar by the curve endomorphism (default), 0: plain windows */
 #define MSM_G1_PARAM_INVERSION 8 /* field inversion of the batched additions: 0 = safegcd divsteps (default),
                                     1 = Fermat a^(p-2) (slower; kept for comparison) */
+#define MSM_G1_PARAM_GRAPH 9   /* 1 (default): msm_g1_run of fewer than 2^19 points captures its launches as a
+                                  CUDA graph on the context's own stream and replays it while the pointers,
+                                  n, window_c and the parameters stay the same (setting any parameter drops
+                                  the graph); 0: every run launches its kernels directly */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 

@@ -519,3 +519,43 @@ def test_config5_adversarial_n2p20(glv):
     pts = points_from_r(r)
     got = run_gpu(pts, k, 16, max_n=n, max_c=16, glv=glv)
     assert np.array_equal(got, oracle.closed_form(r, k))
+
+
+def test_graph_replay_follows_buffer_contents_and_arguments():
+    """Small MSMs replay a captured CUDA graph while the pointers, n and c stay
+    the same: new scalar values in the same buffer, a new output buffer, a
+    parameter change (which drops the graph), the graph switched off, and a run
+    captured inside the caller's own CUDA graph all give the oracle's result."""
+    n, c = 1000, 8
+    cx = gm.MsmG1(n, c)
+    r, k = synth.uniform_workload(n, 4242)
+    pts = gpu_points(points_from_r(r))
+    scal = gpu_scalars(k)
+    out = torch.empty(24, dtype=torch.int32, device="cuda")
+    for step in range(3):
+        cx.run(pts, scal, c, out=out)
+        assert np.array_equal(normalise(out), oracle.closed_form(r, k)), step
+        if step == 0:  # the same buffer, new values: the replay reads them
+            k = synth.uniform_workload(n, 4243)[1]
+            scal.copy_(gpu_scalars(k))
+    out2 = torch.empty(24, dtype=torch.int32, device="cuda")
+    cx.run(pts, scal, c, out=out2)
+    assert np.array_equal(normalise(out2), oracle.closed_form(r, k))
+    cx.set_param(gm.PARAM_GROUPS, 1)
+    cx.run(pts, scal, c, out=out2)
+    assert np.array_equal(normalise(out2), oracle.closed_form(r, k))
+    cx.set_param(gm.PARAM_GRAPH, 0)
+    cx.run(pts, scal, c, out=out)
+    assert np.array_equal(normalise(out), oracle.closed_form(r, k))
+    cx.set_param(gm.PARAM_GRAPH, 1)
+    cx.set_param(gm.PARAM_GROUPS, 0)
+    # inside the caller's capture the run becomes part of the caller's graph
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cx.run(pts, scal, c, out=out, stream=s)
+    out.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    assert np.array_equal(normalise(out), oracle.closed_form(r, k))
