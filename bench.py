@@ -372,6 +372,11 @@ def run_gpu(args, cfg):
                                       "block share one inversion pass (warp 0)" % (
                              "Fermat a^(p-2)" if args.inversion else "safegcd (Bernstein-Yang divsteps)",
                              args.batch_s or 64),
+                         # the count the scope table names: 6 field multiplications of 136 full
+                         # limb products (272 slots) per addition, inversions by divsteps adding
+                         # no multiplications (Fermat runs report null here)
+                         "frac_count_6x272": None if args.inversion else
+                         adds_l0 * 6 * 272 / (l0_ms / 1e3) / 1e12 / peak_timad,
                          "accumulation_frac_all_levels": adds_total * IMAD_SLOTS_PER_ADD
                          / (acc_ms / 1e3) / 1e12 / peak_timad},
             "cpu_baseline": cpu,
