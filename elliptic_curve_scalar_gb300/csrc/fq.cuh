@@ -206,7 +206,10 @@ __device__ __forceinline__ void mac_row_p(uint32_t* T, uint32_t& cin, uint32_t m
 // of limb i+8 belongs to limb i+9 and enters the next round's chain there.
 // T stays below p^2 + p R < 2^511, so limb 16 and the last carry are zero, and
 // T / R < 2p needs one conditional subtraction.
-__device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
+// The same without the final conditional subtraction: the result lies in
+// [0, 2p) and is congruent to a b R^-1.  Valid whenever a b < p R, e.g. for
+// a, b < 2p (4 p < R = 2^256), so such values may feed further lazy products.
+__device__ __forceinline__ fe mul_lazy_inline(const fe& a, const fe& b) {
     uint32_t T[17];
 #pragma unroll
     for (int i = 0; i < 17; i++) T[i] = 0;
@@ -223,6 +226,11 @@ __device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
     fe r;
 #pragma unroll
     for (int j = 0; j < 8; j++) r.v[j] = T[8 + j];
+    return r;
+}
+
+__device__ __forceinline__ fe mul_inline(const fe& a, const fe& b) {
+    fe r = mul_lazy_inline(a, b);
     reduce_once(r);
     return r;
 }
@@ -383,6 +391,7 @@ __device__ __forceinline__ fe sqr_inline(const fe& a) {
 // makes the caller store the operand to its stack frame and the callee load it
 // back, two round trips through local memory per multiplication.
 static __device__ __noinline__ fe mul(fe a, fe b) { return mul_inline(a, b); }
+static __device__ __noinline__ fe mul_lazy(fe a, fe b) { return mul_lazy_inline(a, b); }
 
 // sqr_fused (called, like mul) issues fewer multiply-pipe slots but its three
 // chains (rows, doubling, diagonal) are more serial than a multiplication's

@@ -263,6 +263,14 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
 // accumulation kernels choose); inlining all six was slower still.
 // inv_kind selects the batch inversion: 0 = safegcd divsteps (the default),
 // 1 = Fermat (a^(p-2), 4-bit windows) -- kept for the measured comparison.
+// The three products of Montgomery's trick (the prefix, and the backward pair)
+// skip the final conditional subtraction (fq::mul_lazy_inline): the chain's
+// values stay below 2p, which every product of the chain and the slope's
+// multiplication accept, and both inversions take any representative.  This
+// is the lighter-reduction lever for the batch inversion that the pages list
+// as a next direction (PR #23736 "stream-walker -- amortize the field
+// inversion via large S + private pref_scratch", section "Honest status --
+// NOT done").
 // With sh (shared scratch of 8 x blockDim.x words) the block's threads share
 // one inversion (block_inverse): then every thread of the block must call,
 // those without pairs with count = 0.
@@ -280,7 +288,7 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
         int cs = pair_case(hq, xp, xq, [&](fe& a, fe& b) { src.ys(k, a, b); }, yp);
         fe d = pair_denominator(cs, xp, xq, yp);
         adds += (cs == PC_ADD || cs == PC_DBL);
-        acc = (k == 0) ? d : fq::mul_inline(acc, d);
+        acc = (k == 0) ? d : fq::mul_lazy_inline(acc, d);
         pre[k] = acc;
     }
     fe inv = sh ? block_inverse(acc, sh, inv_kind) : inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
@@ -295,11 +303,11 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
         fe dinv = inv;
         if (k > 0) {
             if (INLINE_BACK) {
-                dinv = fq::mul_inline(inv, pre[k - 1]);
-                inv = fq::mul_inline(inv, d);
+                dinv = fq::mul_lazy_inline(inv, pre[k - 1]);
+                inv = fq::mul_lazy_inline(inv, d);
             } else {
-                dinv = fq::mul(inv, pre[k - 1]);
-                inv = fq::mul(inv, d);
+                dinv = fq::mul_lazy(inv, pre[k - 1]);
+                inv = fq::mul_lazy(inv, d);
             }
         }
         src.store(k, pair_result(cs, p, q, dinv));
