@@ -639,7 +639,7 @@ struct msm_g1_ctx {
     cudaStream_t cap_stream;      // where runs are captured and replayed
     cudaEvent_t ev_in, ev_out;    // the caller's stream -> cap_stream -> the caller's stream
     cudaGraphExec_t gexec;
-    const void* gkey_ptr[3];      // points, scalars, out
+    const void* gkey_ptr[4];      // points, scalars, out, and 1 for the host-buffer entry
     size_t gkey_n;
     int gkey_c;
     int sms;               // streaming multiprocessors of the device
@@ -1289,13 +1289,23 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
 // Small MSMs are a few dozen short, latency-bound launches; replayed as one
 // CUDA graph they start back to back (GB300: n = 2^10 0.655 -> 0.592 ms, 2^16
 // 1.057 -> 0.992 ms per MSM; at 2^20 the graph was 2 % slower, so larger
-// MSMs launch eagerly).  The run is captured on the context's capture stream
-// the first time a (points, scalars, out, n, c) combination is seen -- an
+// MSMs launch eagerly).  A call of msm_g1_run (or of msm_g1_run_host, with its
+// copies, when its host buffers are page-locked) is captured on the context's
+// capture stream the first time a (points, scalars, out, n, c) combination is seen -- an
 // existing executable graph is updated in place when the launches keep their
 // shape -- and replayed while the arguments and the parameters stay the same;
 // the buffers' contents may change between calls, since the kernels read them
 // when they run.  Not while the caller's own stream is being captured (the run
 // then becomes part of the caller's graph as usual).
+static bool pinned(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
 static bool graph_eligible(const msm_g1_ctx* c, size_t n, cudaStream_t st) {
     if (!c->graph_on || !c->streams_ok || c->timing || n == 0 || n >= ((size_t)1 << 19)) return false;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -1306,16 +1316,18 @@ static bool graph_eligible(const msm_g1_ctx* c, size_t n, cudaStream_t st) {
     return cs == cudaStreamCaptureStatusNone;
 }
 
-static int run_graph(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, size_t n, int window_c,
-                     uint32_t* out, cudaStream_t st) {
-    const bool hit = c->gexec && c->gkey_ptr[0] == points && c->gkey_ptr[1] == scalars && c->gkey_ptr[2] == out &&
-                     c->gkey_n == n && c->gkey_c == window_c;
+// body(stream) enqueues the whole call on `stream`; key names its arguments.
+template <class Body>
+static int run_graph(msm_g1_ctx* c, const void* const (&key)[4], size_t n, int window_c, cudaStream_t st,
+                     Body&& body) {
+    bool hit = c->gexec && c->gkey_n == n && c->gkey_c == window_c;
+    for (int i = 0; i < 4; i++) hit = hit && c->gkey_ptr[i] == key[i];
     if (!hit) {
         if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
             cudaGetLastError();
-            return run_core(c, points, scalars, n, window_c, out, st, nullptr);
+            return body(st);
         }
-        const int rc = run_core(c, points, scalars, n, window_c, out, c->cap_stream, nullptr);
+        const int rc = body(c->cap_stream);
         cudaGraph_t g = nullptr;
         const cudaError_t ec = cudaStreamEndCapture(c->cap_stream, &g);
         if (rc != MSM_G1_OK || ec != cudaSuccess || !g) {
@@ -1337,9 +1349,7 @@ static int run_graph(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scal
             return MSM_G1_ERR_CUDA;
         }
         cudaGraphDestroy(g);
-        c->gkey_ptr[0] = points;
-        c->gkey_ptr[1] = scalars;
-        c->gkey_ptr[2] = out;
+        for (int i = 0; i < 4; i++) c->gkey_ptr[i] = key[i];
         c->gkey_n = n;
         c->gkey_c = window_c;
     }
@@ -1355,8 +1365,12 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
                           uint32_t* out, cudaStream_t st) {
     if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
     if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
-    if (graph_eligible(c, n, st)) return run_graph(c, points, scalars, n, window_c, out, st);
-    return run_core(c, points, scalars, n, window_c, out, st, nullptr);
+    auto body = [&](cudaStream_t s) { return run_core(c, points, scalars, n, window_c, out, s, nullptr); };
+    if (graph_eligible(c, n, st)) {
+        const void* const key[4] = {points, scalars, out, nullptr};
+        return run_graph(c, key, n, window_c, st, body);
+    }
+    return body(st);
 }
 
 extern "C" int msm_g1_run_batch(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scalars, const size_t* offsets,
@@ -1429,13 +1443,22 @@ extern "C" int msm_g1_run_host(msm_g1_ctx* c, const uint32_t* points_host, const
     uint32_t* pts = c->stage;
     uint32_t* sc = c->stage + 16 * c->stage_n;
     uint32_t* res = c->stage + 24 * c->stage_n;  // 96 B, 16-byte aligned (offset 96 max_n)
-    if (n > 0) CK(cudaMemcpyAsync(sc, scalars_host, 32ull * n, cudaMemcpyHostToDevice, st));
-    // the points are copied by run_core beside the sort (in order on st when
-    // the context has no streams or times phases)
-    int rc = run_core(c, pts, sc, n, window_c, res, st, n > 0 ? points_host : nullptr);
-    if (rc != MSM_G1_OK) return rc;
-    CK(cudaMemcpyAsync(out_host, res, 96, cudaMemcpyDeviceToHost, st));
-    return MSM_G1_OK;
+    auto body = [&](cudaStream_t s) -> int {
+        if (n > 0) CK(cudaMemcpyAsync(sc, scalars_host, 32ull * n, cudaMemcpyHostToDevice, s));
+        // the points are copied by run_core beside the sort (in order on s when
+        // the context has no streams or times phases)
+        int rc = run_core(c, pts, sc, n, window_c, res, s, n > 0 ? points_host : nullptr);
+        if (rc != MSM_G1_OK) return rc;
+        CK(cudaMemcpyAsync(out_host, res, 96, cudaMemcpyDeviceToHost, s));
+        return MSM_G1_OK;
+    };
+    // replayed as a graph like msm_g1_run, when all three host buffers are
+    // page-locked (copies of pageable memory cannot be captured)
+    if (graph_eligible(c, n, st) && pinned(points_host) && pinned(scalars_host) && pinned(out_host)) {
+        const void* const key[4] = {points_host, scalars_host, out_host, (const void*)1};
+        return run_graph(c, key, n, window_c, st, body);
+    }
+    return body(st);
 }
 
 extern "C" int msm_g1_last_phase_ms(msm_g1_ctx* c, float* ms, int nphase) {

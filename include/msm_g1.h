@@ -66,8 +66,9 @@ extern "C" {
 #define MSM_G1_PARAM_GLV 7     /* 1: split every scalar by the curve endomorphism (default), 0: plain windows */
 #define MSM_G1_PARAM_INVERSION 8 /* field inversion of the batched additions: 0 = safegcd divsteps (default),
                                     1 = Fermat a^(p-2) (slower; kept for comparison) */
-#define MSM_G1_PARAM_GRAPH 9   /* 1 (default): msm_g1_run of fewer than 2^19 points captures its launches as a
-                                  CUDA graph on the context's own stream and replays it while the pointers,
+#define MSM_G1_PARAM_GRAPH 9   /* 1 (default): msm_g1_run of fewer than 2^19 points (and msm_g1_run_host, when
+                                  its three host buffers are page-locked) captures its launches and copies as
+                                  a CUDA graph on the context's own stream and replays it while the pointers,
                                   n, window_c and the parameters stay the same (setting any parameter drops
                                   the graph); 0: every run launches its kernels directly */
 

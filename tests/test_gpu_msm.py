@@ -559,3 +559,31 @@ def test_graph_replay_follows_buffer_contents_and_arguments():
     torch.cuda.synchronize()
     g.replay()
     assert np.array_equal(normalise(out), oracle.closed_form(r, k))
+
+
+def test_graph_replay_of_host_buffer_runs():
+    """msm_g1_run_host with page-locked buffers replays its captured copies and
+    launches: new scalar values in the same host buffer, a new result buffer,
+    and pageable buffers (which take the direct path) all give the oracle's
+    result."""
+    n, c = 900, 9
+    cx = gm.MsmG1(n, c)
+    r, k = synth.uniform_workload(n, 5151)
+    pts = gpu_points(points_from_r(r)).cpu().pin_memory()
+    scal = gpu_scalars(k).cpu().pin_memory()
+    out = torch.empty(24, dtype=torch.int32).pin_memory()
+    for step in range(3):
+        cx.run_host(pts, scal, c, out=out)
+        torch.cuda.synchronize()
+        assert np.array_equal(oracle.jacobian_mont_to_affine(out.numpy().view(np.uint32)), oracle.closed_form(r, k)), step
+        if step == 0:
+            k = synth.uniform_workload(n, 5152)[1]
+            scal.copy_(gpu_scalars(k).cpu())
+    out2 = torch.empty(24, dtype=torch.int32).pin_memory()
+    cx.run_host(pts, scal, c, out=out2)
+    torch.cuda.synchronize()
+    assert np.array_equal(oracle.jacobian_mont_to_affine(out2.numpy().view(np.uint32)), oracle.closed_form(r, k))
+    out3 = torch.empty(24, dtype=torch.int32)
+    cx.run_host(pts.clone(), scal.clone(), c, out=out3)
+    torch.cuda.synchronize()
+    assert np.array_equal(oracle.jacobian_mont_to_affine(out3.numpy().view(np.uint32)), oracle.closed_form(r, k))
