@@ -44,6 +44,13 @@ namespace fq {
 #define FQ_R6 0x9a07df2fu
 #define FQ_R7 0x0e0a77c1u
 
+// Montgomery forms of 2, 3, 8 and 12 (k R mod p), so that a product by one of
+// them is the plain multiple
+#define FQ_MONT2 0x8b1e1b3au, 0xa6ba871bu, 0xeb8e167bu, 0x14f1d651u, 0xf0f28c58u, 0xccdd46deu, 0x340fbe5eu, 0x1c14ef83u
+#define FQ_MONT3 0x50ad28d7u, 0x7a17caa9u, 0xe15521b9u, 0x1f6ac17au, 0x696bd284u, 0x334bea4eu, 0xce179d8eu, 0x2a1f6744u
+#define FQ_MONT8 0x7b7e725au, 0x22a90440u, 0xdd54c4d4u, 0x24c48424u, 0xc0c780a5u, 0xc2d4900eu, 0x0ddbb927u, 0x0f8b2127u
+#define FQ_MONT12 0xb93dab87u, 0x33fd8660u, 0x4bff273eu, 0xb726c637u, 0x212b40f7u, 0xa43ed816u, 0x94c995bbu, 0x1750b1bau
+
 struct fe {
     uint32_t v[8];
 };

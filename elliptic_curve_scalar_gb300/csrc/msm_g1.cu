@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uin
         jac acc = g1::load_jac(src);
         for (uint32_t p = 1; p < parts; p++) acc = g1c::add(acc, g1::load_jac(src + p * 24));
         const uint32_t shift = q == 0 ? 0 : q - 1 + log2L;
-        for (uint32_t i = 0; i < shift; i++) acc = g1c::dbl(acc);
+        acc = g1c::dbl_n(acc, (int)shift);
         __syncwarp();
         if (lane == 0) g1::store_jac(sm + q * 24, acc);
     }
@@ -528,7 +528,7 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
     jac q = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
     for (int w = first ? w_hi - 2 : w_hi - 1; w >= w_lo; w--) {
         // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
-        for (int i = window_width(L, w); i > 0; i--) q = g1c::dbl(q);
+        q = g1c::dbl_n(q, window_width(L, w));
         q = g1c::add(q, g1::load_jac(wsums + (size_t)w * 24));
     }
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
@@ -543,7 +543,7 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
 __global__ void k_combine_shift(uint32_t* __restrict__ acc, int bits) {
     if (blockIdx.x != 0 || threadIdx.x >= 32) return;
     jac q = g1::load_jac(acc);
-    for (int i = 0; i < bits; i++) q = g1c::dbl(q);
+    q = g1c::dbl_n(q, bits);
     if (threadIdx.x == 0) g1::store_jac(acc, q);
 }
 
@@ -560,7 +560,7 @@ __global__ void k_combine_batch(const uint32_t* __restrict__ wsums, Windows L, u
     const uint32_t* ws = wsums + (size_t)m * L.W * 24;
     jac q = g1::load_jac(ws + (size_t)(L.W - 1) * 24);
     for (int w = L.W - 2; w >= 0; w--) {
-        for (int i = window_width(L, w); i > 0; i--) q = g1c::dbl(q);
+        q = g1c::dbl_n(q, window_width(L, w));
         q = g1c::add(q, g1::load_jac(ws + (size_t)w * 24));
     }
     if (threadIdx.x == 0) g1::store_jac(out + (size_t)m * 24, q);

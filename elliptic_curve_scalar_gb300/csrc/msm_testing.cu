@@ -55,6 +55,8 @@ __global__ void k_test_g1_coop(int op, const uint32_t* a, const uint32_t* b, uin
     jac r;
     if (op == MSM_G1_TEST_JAC_DBL_COOP || op == MSM_G1_TEST_JAC_DBL_COOP8)
         r = g1c::dbl<W>(g1::load_jac(a + 24 * i));
+    else if (op == MSM_G1_TEST_JAC_DBL5_COOP)
+        r = g1c::dbl_n<W>(g1::load_jac(a + 24 * i), 5);
     else if (op == MSM_G1_TEST_JAC_ADD_COOP || op == MSM_G1_TEST_JAC_ADD_COOP8)
         r = g1c::add<W>(g1::load_jac(a + 24 * i), g1::load_jac(b + 24 * i));
     else
@@ -134,12 +136,12 @@ extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint
 
 extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_MIXED_COOP8) return MSM_G1_ERR_INVALID_ARG;
+    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_DBL5_COOP) return MSM_G1_ERR_INVALID_ARG;
     bool needs_b = op != MSM_G1_TEST_JAC_DBL && op != MSM_G1_TEST_TO_AFFINE && op != MSM_G1_TEST_JAC_DBL_COOP &&
-                   op != MSM_G1_TEST_JAC_DBL_COOP8;
+                   op != MSM_G1_TEST_JAC_DBL_COOP8 && op != MSM_G1_TEST_JAC_DBL5_COOP;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
-    if (op >= MSM_G1_TEST_JAC_DBL_COOP8)
+    if (op >= MSM_G1_TEST_JAC_DBL_COOP8 && op <= MSM_G1_TEST_JAC_MIXED_COOP8)
         k_test_g1_coop<8><<<(unsigned)((n * 8 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
     else if (op >= MSM_G1_TEST_JAC_DBL_COOP)
         k_test_g1_coop<32><<<(unsigned)((n * 32 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);

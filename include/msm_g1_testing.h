@@ -34,7 +34,8 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
  * into an affine out (16 uint32).  *_COOP are the cooperative doubling,
  * addition and mixed addition of the window combination (one warp per
  * element); *_COOP8 the same with one group of 8 lanes per element, as the
- * bucket reduction runs them (four elements per warp). */
+ * bucket reduction runs them (four elements per warp); DBL5_COOP one warp per
+ * element. */
 #define MSM_G1_TEST_JAC_DBL 0
 #define MSM_G1_TEST_JAC_ADD 1
 #define MSM_G1_TEST_JAC_MIXED 2
@@ -45,6 +46,7 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 #define MSM_G1_TEST_JAC_DBL_COOP8 7
 #define MSM_G1_TEST_JAC_ADD_COOP8 8
 #define MSM_G1_TEST_JAC_MIXED_COOP8 9
+#define MSM_G1_TEST_JAC_DBL5_COOP 10 /* five doublings in a row ([32] a) by the window combination's chain */
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i
