@@ -715,12 +715,15 @@ static uint64_t level_cap(uint64_t h_ub, uint64_t nb, int l) {
 }
 
 // Automatic small-bucket threshold: small MSMs are latency-bound in the
-// narrow tail of the pair tree, large ones are throughput-bound throughout.
+// narrow tail of the pair tree, large ones are throughput-bound throughout
+// (GB300 with the cooperative reduction: n = 2^16, T = 2 / 4 / 8 / 16: 0.912 /
+// 0.926 / 0.898 / 0.977 ms; 2^10, T = 4 / 8 / 16: 0.549 / 0.545 / 0.538 ms;
+// from 2^20 every T >= 2 was slower).
 static int auto_finish(uint64_t n, int W, uint64_t resident) {
     const uint64_t pairs1 = n * (uint64_t)W / 4;  // about the level-1 pairs
     if (pairs1 >= 8 * resident) return 1;
-    if (pairs1 >= 2 * resident) return 4;
-    return 8;
+    if (pairs1 >= 2 * resident) return 8;
+    return 16;
 }
 
 // Window groups (top windows first) and their pair-list layout.
