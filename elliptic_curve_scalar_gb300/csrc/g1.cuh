@@ -34,8 +34,6 @@ __device__ __forceinline__ jac to_jac(const aff& p) {
     return jac{p.x, p.y, fq::one()};
 }
 
-__device__ __forceinline__ aff aff_neg(const aff& p) { return aff{p.x, fq::neg(p.y)}; }
-
 // dbl-2009-l: A = X^2, B = Y^2, C = B^2, D = 2((X+B)^2 - A - C), E = 3A,
 // F = E^2, X3 = F - 2D, Y3 = E(D - X3) - 8C, Z3 = 2YZ.  Infinity maps to
 // infinity (Z3 = 0); no finite point has Y = 0.
@@ -118,20 +116,6 @@ __device__ __forceinline__ aff to_aff(const jac& p) {
     fe zi = inv::inv_safegcd(p.Z);
     fe zi2 = fq::sqr(zi);
     return aff{fq::mul(p.X, zi2), fq::mul(p.Y, fq::mul(zi2, zi))};
-}
-
-// [k]P for a small non-negative integer k (double and add, most significant bit first)
-__device__ __forceinline__ jac mul_small(const jac& p, uint32_t k) {
-    jac acc = jac_inf();
-    if (k == 0) return acc;
-    int top = 31 - __clz(k);
-    acc = p;
-#pragma unroll 1
-    for (int b = top - 1; b >= 0; b--) {
-        acc = dbl(acc);
-        if ((k >> b) & 1) acc = add(acc, p);
-    }
-    return acc;
 }
 
 __device__ __forceinline__ aff load_aff(const uint32_t* p) { return aff{fq::load(p), fq::load(p + 8)}; }
