@@ -310,9 +310,11 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
 }
 
 // the register-capped build once the work fills a resident wave of the other
-// in chunks of min(S, 32)
-static bool wide(uint64_t work, int S, const Resident& res) {
-    const uint64_t s = (uint64_t)std::min(S, 32);
+// in chunks of min(S, per); tree levels switch from 8 pairs per resident
+// thread on (n = 2^20: 3.84 -> 3.79 ms, adversarial 2.90 -> 2.86 ms), level 0
+// from 32 (the single wave of level 0 at n = 2^16 was 5 % slower wide)
+static bool wide(uint64_t work, int S, const Resident& res, int per) {
+    const uint64_t s = (uint64_t)std::min(S, per);
     return (work + s - 1) / s >= res.narrow;
 }
 
@@ -326,7 +328,7 @@ template <int S>
 static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
                      const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
                      ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
-    if (wide(units_ub, S, res))
+    if (wide(units_ub, S, res, 32))
         k_accum_level0_wide<S><<<grid_for(units_ub, S, tpb, res.wide), tpb, 0, st>>>(
             points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
     else
@@ -337,7 +339,7 @@ static void level0_t(int tpb, const Resident& res, const uint32_t* points, const
 template <int S>
 static void list_t(int tpb, const Resident& res, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
                    int grp, int level, int stats, int inv_kind, cudaStream_t st) {
-    if (wide(cap, S, res))
+    if (wide(cap, S, res, 8))
         k_accum_list_wide<S><<<grid_for(cap, S, tpb, res.wide), tpb, 0, st>>>(items, list, ctl, grp, level, stats,
                                                                               inv_kind);
     else
