@@ -311,7 +311,7 @@ static unsigned grid_for(uint64_t work, int S, int tpb, uint64_t resident) {
 
 // the register-capped build once the work fills a resident wave of the other
 // in chunks of min(S, per); tree levels switch from 8 pairs per resident
-// thread on (n = 2^20: 3.84 -> 3.79 ms, adversarial 2.90 -> 2.86 ms), level 0
+// thread on (n = 2^20: 3.67 -> 3.63 ms, adversarial 2.81 -> 2.79 ms), level 0
 // from 32 (the single wave of level 0 at n = 2^16 was 5 % slower wide)
 static bool wide(uint64_t work, int S, const Resident& res, int per) {
     const uint64_t s = (uint64_t)std::min(S, per);
