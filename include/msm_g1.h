@@ -26,7 +26,10 @@
  *                    Values >= r are allowed and act as k mod r, because every
  *                    point of E(F_p) has order dividing r.
  *   result, Jacobian: 24 x uint32: X[8], Y[8], Z[8] in Montgomery form,
- *                    representing (X/Z^2, Y/Z^3); Z = 0 is infinity.
+ *                    representing (X/Z^2, Y/Z^3); Z = 0 is infinity.  The
+ *                    point is exact; its Jacobian representative may differ
+ *                    between runs (the order of a bucket's entries follows
+ *                    the device's atomics), so compare results in affine form.
  *
  * Errors: every entry point returns 0 on success or a negative MSM_G1_ERR_*
  * code; argument errors are detected on the host before any device work is
