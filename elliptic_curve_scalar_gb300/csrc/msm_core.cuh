@@ -194,18 +194,21 @@ __device__ __forceinline__ aff pair_result(int cs, const aff& p, const aff& q, c
 
 // One inversion per block instead of one per warp.  Every thread of the block
 // brings one nonzero value a (its batch's product; 1 when it has no batch)
-// and receives a^-1.  Warp 0 gathers the block's values through shared memory
-// (sh: 8 x blockDim.x words, word w of value i at sh[w * blockDim.x + i], so
-// that consecutive lanes hit consecutive banks), lane j taking the g =
-// blockDim.x / 32 values j, j + 32, ...; it runs Montgomery's trick over its
-// g values, inverts the 32 group products in one pass of the per-lane
-// inversion, and writes the inverses back.  The other warps wait at the
-// barrier: the block issues one warp's inversion where each warp used to issue
-// its own, which at small batches (a launch of one wave, 9 additions per
-// thread at n = 2^16) is a quarter of the instructions that dominate
-// (divsteps on the ALU pipe, their 64-bit updates on the multiply pipe).
-// All threads of the block must call it; blockDim.x is a multiple of 32 and
-// at most 256.
+// and receives a^-1.  The block's warps multiply their values pairwise in a
+// tree (level s: warp w < s multiplies lane by lane with warp w + s, whose
+// values it reads from shared memory), warp 0 inverts the 32 products of all
+// warps in one pass of the per-lane inversion, and the tree is walked back
+// down (warp w < s hands warp w + s its inverse through shared memory): with
+// four warps, two multiplications up and two levels of two independent ones
+// down, where a single warp gathering the block's values needed nine in a row.
+// The other warps wait at the barriers while warp 0 inverts: the block issues
+// one warp's inversion where each warp used to issue its own, which at small
+// batches (a launch of one wave, 9 additions per thread at n = 2^16) is a
+// quarter of the instructions that dominate (divsteps on the ALU pipe, their
+// 64-bit updates on the multiply pipe).  sh: 8 x blockDim.x words, word w of
+// thread i's slot at sh[w * blockDim.x + i] (consecutive lanes hit consecutive
+// banks).  All threads of the block must call it; blockDim.x is a multiple of
+// 32 and at most 256.
 __device__ __forceinline__ void sh_store(uint32_t* sh, int i, const fe& a) {
 #pragma unroll
     for (int w = 0; w < 8; w++) sh[w * blockDim.x + i] = a.v[w];
@@ -218,30 +221,30 @@ __device__ __forceinline__ fe sh_load(const uint32_t* sh, int i) {
 }
 
 __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_kind) {
-    const int tid = threadIdx.x;
-    sh_store(sh, tid, a);
-    __syncthreads();
-    if (tid < 32) {
-        const int g = blockDim.x >> 5;
-        fe pre[8];
-        fe acc = sh_load(sh, tid);
-        pre[0] = acc;
-#pragma unroll 1
-        for (int i = 1; i < g; i++) {
-            acc = fq::mul(acc, sh_load(sh, tid + 32 * i));
-            pre[i] = acc;
+    const int tid = threadIdx.x, warp = tid >> 5, nw = blockDim.x >> 5;
+    fe v = a;
+    fe keep[3];  // this warp's values below each level it multiplied at (nw <= 8)
+    int lv = 0;
+    for (int s = nw >> 1; s >= 1; s >>= 1, lv++) {
+        if (warp >= s && warp < 2 * s) sh_store(sh, tid, v);
+        __syncthreads();
+        if (warp < s) {
+            keep[lv] = v;
+            v = fq::mul(v, sh_load(sh, tid + 32 * s));
         }
-        fe inv = inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
-#pragma unroll 1
-        for (int i = g - 1; i > 0; i--) {
-            const fe v = sh_load(sh, tid + 32 * i);
-            sh_store(sh, tid + 32 * i, fq::mul(inv, pre[i - 1]));
-            inv = fq::mul(inv, v);
-        }
-        sh_store(sh, tid, inv);
     }
-    __syncthreads();
-    return sh_load(sh, tid);
+    if (warp == 0) v = inv_kind ? fq::inv_fermat(v) : inv::inv_safegcd(v);
+    for (int s = 1; s < nw; s <<= 1) {
+        lv--;
+        if (warp < s) {
+            const fe partner = sh_load(sh, tid + 32 * s);
+            sh_store(sh, tid + 32 * s, fq::mul(v, keep[lv]));
+            v = fq::mul(v, partner);
+        }
+        __syncthreads();
+        if (warp >= s && warp < 2 * s) v = sh_load(sh, tid);
+    }
+    return v;
 }
 
 // Run one batch of up to S pair additions.  Src supplies, per slot k < count:
