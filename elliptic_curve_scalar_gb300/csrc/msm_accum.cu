@@ -77,7 +77,7 @@ struct Level0Src {
 
 // Each accumulation kernel comes in two builds of one body: at its natural
 // register count (about 100), and capped at 80 registers ("wide": 6 blocks of
-// 128 threads per SM instead of 4, for a few spilled words).  The wide build
+// 128 threads per SM instead of 4; it spilled a few words when introduced).  The wide build
 // is used when a launch has at least a resident wave of work, where the extra
 // warps hide latency (n = 2^22 on GB300: 14.17 -> 13.29 ms per MSM; caps of
 // 96, 88, 72 and 64 were slower); small launches are latency-bound and the
