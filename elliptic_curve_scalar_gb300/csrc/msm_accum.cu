@@ -78,10 +78,11 @@ struct Level0Src {
 // Each accumulation kernel comes in two builds of one body: at its natural
 // register count (about 100), and capped at 80 registers ("wide": 6 blocks of
 // 128 threads per SM instead of 4; it spilled a few words when introduced).  The wide build
-// is used when a launch has at least a resident wave of work, where the extra
-// warps hide latency (n = 2^22 on GB300: 14.17 -> 13.29 ms per MSM; caps of
-// 96, 88, 72 and 64 were slower); small launches are latency-bound and the
-// spills only add latency there (n = 2^16: 1.27 vs 1.32 ms).
+// is used for launches with enough work per resident thread (wide() below),
+// where the extra warps hide latency (n = 2^22 on GB300: 14.17 -> 13.29 ms per
+// MSM; caps of 96, 88, 72 and 64 were slower); small launches are
+// latency-bound and the cap only adds latency there (n = 2^16: 1.27 vs 1.32 ms
+// when introduced).
 #define LEVEL0_PARAMS                                                                                     \
     const uint32_t *__restrict__ points, const uint32_t *__restrict__ phi, uint32_t nsplit,                \
         const uint32_t *__restrict__ entries, const uint32_t *__restrict__ offsets, uint32_t g0, uint32_t g1, \
