@@ -844,6 +844,27 @@ static size_t layout(msm_g1_ctx* c, const sizing& s, bool assign) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
+// Makes a context's device current for one entry point and gives the caller
+// back its own current device on return, so a call never moves the caller's
+// thread to another GPU.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            prev = -1;
+            return;
+        }
+        ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+    DeviceGuard(const DeviceGuard&) = delete;
+    DeviceGuard& operator=(const DeviceGuard&) = delete;
+};
+
 #define CK(call)                                  \
     do {                                          \
         if ((call) != cudaSuccess) return MSM_G1_ERR_CUDA; \
@@ -956,6 +977,7 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
 
 void msm_g1_destroy(msm_g1_ctx* c) {
     if (!c) return;
+    const DeviceGuard dg(c->device);
     cudaDeviceSynchronize();
     if (c->events_made)
         for (int i = 0; i <= kPhases; i++) cudaEventDestroy(c->ev[i]);
@@ -1079,7 +1101,6 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
             return MSM_G1_ERR_CAPACITY;
     }
     const BatchMap bm{count > 1 ? d_off : nullptr, count};
-    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
     c->have_timing = false;
     if (c->timing && !c->events_made) {
         for (int i = 0; i <= kPhases; i++) CK(cudaEventCreate(&c->ev[i]));
@@ -1368,6 +1389,8 @@ extern "C" int msm_g1_run(msm_g1_ctx* c, const uint32_t* points, const uint32_t*
                           uint32_t* out, cudaStream_t st) {
     if (!c || !out || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
     if (n > 0 && (!points || !scalars || !aligned16(points) || !aligned16(scalars))) return MSM_G1_ERR_INVALID_ARG;
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     auto body = [&](cudaStream_t s) { return run_core(c, points, scalars, n, window_c, out, s, nullptr); };
     if (graph_eligible(c, n, st)) {
         const void* const key[4] = {points, scalars, out, nullptr};
@@ -1395,7 +1418,8 @@ extern "C" int msm_g1_run_batch(msm_g1_ctx* c, const uint32_t* points, const uin
     const int W = make_windows(cw, glv ? GLV_BITS : PLAIN_BITS).W;
     const uint64_t B = 1ull << (cw - 1);
     const ReducePlan rp = reduce_plan((uint32_t)B);
-    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     // Greedy passes: as many consecutive MSMs as the context's buffers hold.
     int m0 = 0;
     while (m0 < count) {
@@ -1433,7 +1457,8 @@ extern "C" int msm_g1_run_host(msm_g1_ctx* c, const uint32_t* points_host, const
     if (!c || !out_host) return MSM_G1_ERR_INVALID_ARG;
     if (n > 0 && (!points_host || !scalars_host)) return MSM_G1_ERR_INVALID_ARG;
     if (n > c->max_n) return MSM_G1_ERR_CAPACITY;
-    if (cudaSetDevice(c->device) != cudaSuccess) return MSM_G1_ERR_CUDA;
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     if (!c->stage) {  // first call: device copies of points, scalars and the result, for max_n
         size_t bytes = 96 * c->max_n + 256;
         if (cudaMalloc((void**)&c->stage, bytes) != cudaSuccess) {
@@ -1476,7 +1501,8 @@ extern "C" int msm_g1_last_phase_ms(msm_g1_ctx* c, float* ms, int nphase) {
 extern "C" int msm_g1_last_stats(msm_g1_ctx* c, uint64_t* out, int nout) {
     if (!c || !out || nout < 0) return MSM_G1_ERR_INVALID_ARG;
     ctl_t h;
-    CK(cudaSetDevice(c->device));
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));
     uint64_t v[8] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
@@ -1491,7 +1517,8 @@ extern "C" int msm_g1_mul_generator(msm_g1_ctx* c, const uint32_t* scalars, size
     if (!c) return MSM_G1_ERR_INVALID_ARG;
     if (n == 0) return MSM_G1_OK;
     if (!scalars || !out || !aligned16(scalars) || !aligned16(out)) return MSM_G1_ERR_INVALID_ARG;
-    CK(cudaSetDevice(c->device));
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     if (!c->gen_ready) {
         k_gen_table_jac<<<1, 32, 0, st>>>(c->gen_tj);
         k_gen_table_norm<<<2, 128, 0, st>>>(c->gen_tj, c->gen_table);
@@ -1503,7 +1530,8 @@ extern "C" int msm_g1_mul_generator(msm_g1_ctx* c, const uint32_t* scalars, size
 
 extern "C" int msm_g1_debug_read(msm_g1_ctx* c, int which, void* dst, size_t max_bytes, size_t* bytes) {
     if (!c || !dst || !bytes) return MSM_G1_ERR_INVALID_ARG;
-    CK(cudaSetDevice(c->device));
+    const DeviceGuard dg(c->device);
+    if (!dg.ok) return MSM_G1_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     ctl_t h;
     CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));

@@ -34,7 +34,10 @@
  * Errors: every entry point returns 0 on success or a negative MSM_G1_ERR_*
  * code; argument errors are detected on the host before any device work is
  * queued.  Calls are asynchronous on the given stream unless stated otherwise;
- * a context is not thread-safe (one run at a time per context).
+ * a context is not thread-safe (one run at a time per context).  A call on a
+ * context runs on the device the context was created on, whatever device is
+ * current, and leaves the calling thread's current device as it found it; the
+ * stream passed must belong to the context's device.
  */
 #ifndef MSM_G1_H
 #define MSM_G1_H
