@@ -95,6 +95,18 @@ def dist_setup(backend):
     return world, rank, local
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of the ranks' values of x: every replica's time counts, so the
+    job is as slow as its slowest rank (x itself when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload(cfg):
     from elliptic_curve_scalar_gb300 import synth
     return synth.workload(cfg["kind"], cfg["n"], cfg["seed"])
@@ -116,7 +128,10 @@ def oracle_points_per_s(cfg, sample, threads=None):
 
 def run_reference(args, cfg):
     world, rank, _ = dist_setup("gloo")
-    if rank != 0:
+    if rank != 0:  # the oracle runs once, on rank 0; the other ranks leave without work
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return 0
     sample = 8192
     vals, times = [], []
@@ -139,6 +154,9 @@ def run_reference(args, cfg):
         "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
     return 0
 
 
@@ -259,11 +277,7 @@ def run_gpu(args, cfg):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     value = world * K * n * args.steps / (total_ms / 1000.0)
 
@@ -299,11 +313,7 @@ def run_gpu(args, cfg):
             out_hk.copy_(out_d, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     # roofline of the dominant kernel: level-0 batched affine accumulation
     m = counts.astype(np.int64)
