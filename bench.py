@@ -346,7 +346,7 @@ def run_gpu(args, cfg):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # about 10-30 s of CPU work on a 16-core host (0.8 s wall on the box's 16 Arm cores)
+        # a bounded sample: about 13 core-seconds of oracle work (0.8 s wall on 16 Grace cores)
         sample = 65536
         v, dt, threads = oracle_points_per_s(cfg, sample)
         cpu = {"value": v, "unit": "points/s", "cores": threads, "kind": "oracle",
