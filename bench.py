@@ -15,6 +15,7 @@ Inputs fit in L2 (129 MB), so L2 is flushed (a 256 MiB write) before every
 timed step, outside the step's CUDA events.
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -62,6 +63,45 @@ IMAD_SLOTS_PER_FQ_MUL = 2 * 128 + 8
 IMAD_SLOTS_PER_FQ_SQR = 2 * (36 + 64) + 8
 # 5M + 1S per batched affine addition (prefix, 2 backward, slope, x3 square, y3)
 IMAD_SLOTS_PER_ADD = 5 * IMAD_SLOTS_PER_FQ_MUL + IMAD_SLOTS_PER_FQ_SQR
+
+
+# The level-0 accumulation kernel's translation unit and every header it
+# includes.  profiles/traffic.json holds ncu DRAM counters for one build of the
+# kernel together with the digest of these files at that build; the bench line
+# reports the counters as the roofline's traffic only while the digest matches.
+LEVEL0_SOURCES = ("msm_accum.cu", "msm_internal.cuh", "msm_core.cuh", "g1_coop.cuh", "g1.cuh", "glv.cuh",
+                  "inv.cuh", "fq.cuh")
+
+
+def level0_sources_digest(read=None):
+    """sha256 over LEVEL0_SOURCES (name and contents of each, in order);
+    read(name) -> bytes supplies the contents (default: the working tree)."""
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "elliptic_curve_scalar_gb300", "csrc", name), "rb") as f:
+                return f.read()
+    h = hashlib.sha256()
+    for name in LEVEL0_SOURCES:
+        h.update(name.encode() + b"\0" + read(name) + b"\0")
+    return h.hexdigest()
+
+
+def level0_traffic(config_key, prof=None):
+    """(traffic, earlier): the ncu DRAM bytes of the level-0 launch for this
+    workload when they were taken on the kernel as it is now, else None and
+    the figure of the earlier build (or None when there is none)."""
+    prof = prof or os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(prof) as f:
+            tj = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    val = tj.get(config_key)
+    if val is None:
+        return None, None
+    if tj.get("sources_sha256") == level0_sources_digest():
+        return val, None
+    return None, val
 
 
 def parse():
@@ -333,16 +373,7 @@ def run_gpu(args, cfg):
     peak_timad = sms * IMAD_SLOTS_PER_CLK_PER_SM * sm_max_mhz * 1e6 / 1e12
     strict_imad = adds_l0 * IMAD_SLOTS_PER_ADD
     achieved = strict_imad / (l0_ms / 1e3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                tj = json.load(f)
-            key = "%s_S%s" % (args.config, args.batch_s or "auto")
-            traffic = tj.get(key)
-        except (OSError, ValueError):
-            traffic = None
+    traffic, traffic_earlier = level0_traffic("%s_S%s" % (args.config, args.batch_s or "auto"))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -372,6 +403,9 @@ def run_gpu(args, cfg):
             "serial_ms_per_msm": round(sum(mean_phase.values()), 4),
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_timad, "unit": "TIMADslot/s",
                          "frac": achieved / peak_timad, "traffic": traffic,
+                         # counters of an earlier build of the kernel (its sources changed since
+                         # the capture): context only, hence traffic is null
+                         "traffic_earlier_build": traffic_earlier,
                          "kernel": "k_accum_level0",
                          "peak_basis": "%d SMs x %d IMAD slots/clk x %.0f MHz (sm_max_mhz of MEASURED_PEAKS.json)"
                                        % (sms, IMAD_SLOTS_PER_CLK_PER_SM, sm_max_mhz),
