@@ -3,6 +3,8 @@ its host-side logic (argument checks, sizing helpers) works without a GPU."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -40,6 +42,35 @@ def test_headers_declare_the_boundary():
 @pytest.mark.parametrize("name", declared_functions())
 def test_symbol_exported(lib, name):
     assert hasattr(lib, name), name
+
+
+def _cuda_include():
+    for base in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if base and os.path.exists(os.path.join(base, "include", "cuda_runtime_api.h")):
+            return os.path.join(base, "include")
+    return None
+
+
+def test_headers_compile_and_link_as_c(lib, tmp_path):
+    """The boundary is plain C: the headers compile as C11 (warnings as errors)
+    and a C program links against the library, resolving every declared entry
+    point, then runs the host-only helpers."""
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    inc = _cuda_include()
+    if not gcc or not inc:
+        pytest.skip("no C compiler or CUDA headers")
+    src = os.path.join(ROOT, "tests", "c_abi_check.c")
+    text = open(src).read()
+    for name in declared_functions():
+        assert "(any_fn)%s," % name in text, name
+    libdir = os.path.dirname(lib_build.LIB)
+    exe = str(tmp_path / "c_abi_check")
+    cmd = [gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           "-isystem", inc, src, "-o", exe, "-L", libdir, "-lmsm_g1", "-Wl,-rpath," + libdir]
+    built = subprocess.run(cmd, capture_output=True, text=True)
+    assert built.returncode == 0, built.stdout + built.stderr
+    ran = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert ran.returncode == 0 and "c abi ok" in ran.stdout, (ran.returncode, ran.stdout, ran.stderr)
 
 
 def test_window_count(lib):
