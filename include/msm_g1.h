@@ -170,7 +170,7 @@ int msm_g1_mul_generator(msm_g1_ctx *ctx, const uint32_t *scalars, size_t n, uin
 int msm_g1_run_noalloc(const uint32_t *points_affine, const uint32_t *scalars, size_t n, int window_c,
                        uint32_t *out_jacobian, cudaStream_t stream);
 
-/* Release the context's scratch (synchronises the device first).  NULL is a no-op. */
+/* Release the context's scratch (synchronises the context's device first).  NULL is a no-op. */
 void msm_g1_destroy(msm_g1_ctx *ctx);
 
 /* Set / read a tunable (MSM_G1_PARAM_*).  Takes effect on the next run. */
