@@ -9,6 +9,10 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
+    # temporary files of the tests stay inside the repository (git-ignored)
+    if not config.option.basetemp:
+        os.makedirs(os.path.join(ROOT, "_build"), exist_ok=True)
+        config.option.basetemp = os.path.join(ROOT, "_build", "pytest-tmp")
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: CPU test that takes more than a few seconds")
 
