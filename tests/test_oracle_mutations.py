@@ -1,7 +1,6 @@
 """Plant one mistake at a time in the C oracle (on the CPU) and check that the
 pins reject every variant: evidence that the pins pin the oracle."""
 import os
-import tempfile
 
 import pytest
 
@@ -22,9 +21,8 @@ MUTATIONS = {
 
 
 @pytest.fixture(scope="module")
-def mutant_dir():
-    with tempfile.TemporaryDirectory() as d:
-        yield d
+def mutant_dir(tmp_path_factory):
+    return str(tmp_path_factory.mktemp("oracle_mutants"))
 
 
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS), ids=lambda m: "M%d" % m)
