@@ -207,9 +207,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_uuid=None):
+    def __init__(self, device_uuid=None, tmpdir=None):
         self.proc = None
-        self.file = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False)
+        self.file = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False, dir=tmpdir)
         cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
         if device_uuid:
             cmd += ["-i", device_uuid]
@@ -226,21 +226,29 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
         self.file.close()
-        rows = []
         with open(self.file.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) == 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.file.name)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        return summarize_clocks(lines)
+
+
+def summarize_clocks(lines):
+    """The bench line's "clocks" from nvidia-smi rows of ClockSampler.FIELDS
+    (csv, no header, no units): median SM clock, highest maximum clock, and
+    every throttle reason seen active in any sample."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) == 9:
+            rows.append(parts)
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+    mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower().startswith("active")})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows)}
 
 
 # ------------------------------------------------------------- GPU arm
