@@ -555,8 +555,9 @@ int oracle_g1_is_on_curve(const uint64_t *pt) {
     oracle_init();
     aff p;
     aff_load(&p, pt);
+    if (MUT(9)) return 1;
     if (p.inf) return 1;
-    if (geq_n(p.x.v, FP.m, 4) || geq_n(p.y.v, FP.m, 4)) return 0;
+    if (!MUT(10) && (geq_n(p.x.v, FP.m, 4) || geq_n(p.y.v, FP.m, 4))) return 0;
     fe y2, x3, three = {{3, 0, 0, 0}};
     fe_mul(&FP, &y2, &p.y, &p.y);
     fe_mul(&FP, &x3, &p.x, &p.x);

@@ -10,6 +10,9 @@ The facts:
 * field products and inverses against Python integers (exact, any size);
 * Montgomery encoding x -> x * 2^256 mod p against Python integers;
 * group sanity: G = (1, 2) on y^2 = x^3 + 3, [r]G = infinity, [r-1]G = -G;
+* the curve-membership test rejects what y^2 = x^3 + 3 over F_p excludes: a
+  point with x or y moved by one, (1, 3), and coordinates that are not
+  canonical residues (x + p or y + p in place of x or y);
 * brute force: tiny MSMs against repeated addition with the affine law;
 * all-ones scalars give the plain point sum;
 * closed form: for P_i = [r_i]G the MSM is [sum k_i r_i mod r]G, with the
@@ -86,6 +89,25 @@ def pin_group():
     assert _pt(oracle.scalar_mul(g, oracle.int_to_limbs(2))) == pyref.add(pyref.G, pyref.G), "[2]G"
     big = (1 << 256) - 1
     assert _pt(oracle.scalar_mul(g, oracle.int_to_limbs(big))) == pyref.mul(big % R, pyref.G), "[2^256-1]G"
+
+
+def pin_on_curve_rejects():
+    """Points off y^2 = x^3 + 3, or with a coordinate outside [0, p), are not
+    on the curve; both oracles must say so (the points they accept are
+    covered by pin_group and the pins that check their outputs)."""
+    rng = random.Random(18)
+    _, pts = _rand_points(rng, 3)
+    bad = [(1, 3), (2, 3), (0, 1)]
+    for x, y in pts:
+        bad += [(x, (y + 1) % P), ((x + 1) % P, y), (x + P, y), (x, y + P)]
+        # (x + 1, y) is on the curve only if 3x^2 + 3x + 1 = 0 mod p: never for these seeds
+        assert (y * y - (x + 1) ** 3 - 3) % P != 0
+    for x, y in bad:
+        assert not pyref.on_curve((x, y)), ("pyref.on_curve accepts", x, y)
+        w = np.concatenate([oracle.int_to_limbs(x), oracle.int_to_limbs(y)])
+        assert not oracle.is_on_curve(w), ("is_on_curve accepts", x, y)
+    for p in pts:
+        assert pyref.on_curve(p) and oracle.is_on_curve(oracle.point_to_words(p))
 
 
 def pin_generator_multiples():
@@ -191,6 +213,7 @@ ALL_PINS = [
     pin_field,
     pin_montgomery,
     pin_group,
+    pin_on_curve_rejects,
     pin_generator_multiples,
     pin_brute_force,
     pin_all_ones,

@@ -17,6 +17,8 @@ MUTATIONS = {
     6: "Montgomery decoding multiplies by R instead of R^-1",
     7: "comb table indexed by the wrong byte of the scalar",
     8: "addition of equal points returns infinity instead of doubling",
+    9: "the curve-membership test accepts every point",
+    10: "the curve-membership test skips its range check on the coordinates",
 }
 
 
