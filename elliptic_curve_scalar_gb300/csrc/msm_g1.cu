@@ -657,6 +657,8 @@ struct msm_g1_ctx {
     bool events_made;
     bool have_timing;
     int last_levels;
+    // plan of the last run: small-bucket threshold, buckets per reduction chunk, window groups
+    uint32_t last_finish_t, last_chunk_len, last_groups;
 };
 
 static int window_count(int c) { return make_windows(c, PLAIN_BITS).W; }
@@ -1210,6 +1212,9 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     const ReducePlan rp = reduce_plan(B);
     const uint32_t L = rp.L, G = rp.G;
     if (rp.jobs > MAX_REDUCE_JOBS) return MSM_G1_ERR_INVALID_ARG;  // unreachable for c <= 20
+    c->last_finish_t = lay.finish_t;
+    c->last_chunk_len = L;
+    c->last_groups = (uint32_t)lay.groups;
     // one window group: level 0, the tree levels, the bucket reduction
     auto level0 = [&](int j, cudaStream_t s) {
         if (side) cudaStreamWaitEvent(s, c->ev_points, 0);
@@ -1505,9 +1510,9 @@ extern "C" int msm_g1_last_stats(msm_g1_ctx* c, uint64_t* out, int nout) {
     if (!dg.ok) return MSM_G1_ERR_CUDA;
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(&h, c->ctl, sizeof(h), cudaMemcpyDeviceToHost));
-    uint64_t v[8] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
-                     (uint64_t)c->last_launches, h.error};
-    int k = std::min(nout, 8);
+    uint64_t v[11] = {h.entries, h.nonempty, h.max_count, h.adds, h.inversions, h.levels,
+                      (uint64_t)c->last_launches, h.error, c->last_finish_t, c->last_chunk_len, c->last_groups};
+    int k = std::min(nout, 11);
     for (int i = 0; i < k; i++) out[i] = v[i];
     return k;
 }

@@ -39,7 +39,8 @@ PLAIN_BITS = 255  # bits the signed windows of a scalar mod r cover
 GLV_BITS = 128    # bits the signed windows of one GLV half cover
 
 PHASES = ("digits", "scan", "scatter", "accum_l0", "accum_tree", "bucket_reduce", "combine")
-STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches", "error")
+STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "levels", "launches", "error",
+         "finish_t", "chunk_len", "groups")
 
 TEST_FQ = {"mul": 0, "sqr": 1, "add": 2, "sub": 3, "neg": 4, "inv": 5, "inv_fermat": 6}
 TEST_G1 = {"jac_dbl": 0, "jac_add": 1, "jac_mixed": 2, "to_affine": 3, "jac_dbl_coop": 4, "jac_add_coop": 5,

@@ -190,8 +190,10 @@ int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
  * MSM_G1_PARAM_STATS = 1 also out[3] = affine additions performed by the
  * accumulation, out[4] = field inversions it performed, out[5] = tree levels
  * that had work (zero otherwise); out[6] = kernels the last run launched;
- * out[7] = non-zero if a device-side capacity check failed (never expected).
- * Returns the number of counters written (at most nout). */
+ * out[7] = non-zero if a device-side capacity check failed (never expected);
+ * the last run's plan: out[8] = small-bucket threshold T it used (1 = none),
+ * out[9] = buckets per chunk of the bucket reduction, out[10] = window groups.
+ * Returns the number of counters written (at most nout, at most 11). */
 int msm_g1_last_stats(msm_g1_ctx *ctx, uint64_t *out, int nout);
 
 /* Host-only helpers (no device work). */
