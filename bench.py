@@ -142,6 +142,9 @@ def parse():
     ap.add_argument("--batch-s", type=int, default=0,
                     help="additions per thread batch: 1..64, 0 = the library's choice (64)")
     ap.add_argument("--tpb", type=int, default=128)
+    ap.add_argument("--place", type=int, default=0, choices=[0, 1, 2],
+                    help="prefix products of a batch: 0 thread-local (device memory), 1 shared memory, 2 registers")
+    ap.add_argument("--grid", type=int, default=0, help="most blocks per accumulation launch (0 = automatic)")
     ap.add_argument("--finish", type=int, default=0, help="small-bucket threshold T (0 = automatic)")
     ap.add_argument("--groups", type=int, default=0, help="window groups of the pipelined schedule (0 = library default)")
     ap.add_argument("--glv", type=int, default=1, choices=[0, 1], help="split scalars by the GLV endomorphism")
@@ -439,6 +442,8 @@ def make_context(args, cfg, dev, K, n):
     ctx.set_param(gm.PARAM_GROUPS, args.groups)
     ctx.set_param(gm.PARAM_GLV, args.glv)
     ctx.set_param(gm.PARAM_INVERSION, args.inversion)
+    ctx.set_param(gm.PARAM_ACC_PLACEMENT, args.place)
+    ctx.set_param(gm.PARAM_GRID, args.grid)
     scal_d = gm.to_device(synth.scalars_to_u32(k), dev)
     # points P_i = [r_i]G built on the device by the library's fixed-base kernel
     pts_d = ctx.mul_generator(gm.to_device(synth.scalars_to_u32(r), dev))
@@ -675,6 +680,7 @@ def run_gpu(args, cfg):
                                       " GLV" if args.glv else "", cfg["kind"], cfg["seed"]),
                        "n": n, "c": c, "S": args.batch_s or "auto", "tpb": args.tpb, "kind": cfg["kind"],
                        "glv": args.glv, "batch": K, "finish_t": args.finish or "auto", "groups": args.groups,
+                       "placement": ("local", "shared", "registers")[args.place], "grid": args.grid or "auto",
                        "msms_per_step": reps * K,
                        "l2": "flushed before every timed MSM (256 MiB write, outside its events)",
                        "replicas": world},

@@ -86,50 +86,64 @@ struct Level0Src {
 #define LEVEL0_PARAMS                                                                                     \
     const uint32_t *__restrict__ points, const uint32_t *__restrict__ phi, uint32_t nsplit,                \
         const uint32_t *__restrict__ entries, const uint32_t *__restrict__ offsets, uint32_t g0, uint32_t g1, \
-        uint32_t *__restrict__ items, ctl_t *ctl, int stats, int inv_kind
-#define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind
+        uint32_t *__restrict__ items, ctl_t *ctl, int stats, int inv_kind, uint32_t base
+#define LEVEL0_ARGS points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind, base
 
-template <int S, bool WIDE>
+template <int S, bool WIDE, int PLACE>
 __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
-    // units of buckets [g0, g1): pairs (2u, 2u+1) for u in [offset_g0 / 2, offset_g1 / 2)
+    // units of buckets [g0, g1): pairs (2u, 2u+1) for u in [offset_g0 / 2, offset_g1 / 2);
+    // this launch takes those from `base` on (a grid capped below the work,
+    // MSM_G1_PARAM_GRID, runs as several launches with increasing base)
     const uint32_t ubeg = offsets[g0] >> 1;
-    const uint32_t units = (offsets[g1] >> 1) - ubeg;
+    const uint32_t all = (offsets[g1] >> 1) - ubeg;
+    if (base >= all) return;
+    const uint32_t units = all - base;
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)units + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint64_t u0 = ubeg + t * chunk;
+    const uint64_t u0 = (uint64_t)ubeg + base + t * chunk;
     // the block may share one inversion: a block with work keeps all its threads
     if ((uint64_t)blockIdx.x * blockDim.x * chunk >= units) return;
     const int count = t * chunk < units ? (int)min(chunk, (uint64_t)units - t * chunk) : 0;
+    // narrow launches (one pair per thread) keep per-thread inversions: the
+    // block's shared one would add warp 0's group products to their latency
+    const bool share = chunk >= 2;
+    if (!share && count == 0) return;
     __shared__ uint32_t sh[8 * 256];
+    extern __shared__ uint32_t pre_sh[];  // prefix products with PLACE_SHARED
     Level0Src<S> src;
     src.points = points;
     src.phi = phi;
     src.nsplit = nsplit;
     src.items = items;
     src.u0 = (uint32_t)u0;
-    for (int k = 0; k < count; k++) {
-        uint2 e = reinterpret_cast<const uint2*>(entries)[u0 + k];
-        src.e0[k] = e.x;
-        src.e1[k] = e.y;
+    if constexpr (PLACE == PLACE_REGS) {
+#pragma unroll
+        for (int k = 0; k < S; k++) {
+            uint2 e = k < count ? reinterpret_cast<const uint2*>(entries)[u0 + k] : make_uint2(0, 0);
+            src.e0[k] = e.x;
+            src.e1[k] = e.y;
+        }
+    } else {
+        for (int k = 0; k < count; k++) {
+            uint2 e = reinterpret_cast<const uint2*>(entries)[u0 + k];
+            src.e0[k] = e.x;
+            src.e1[k] = e.y;
+        }
     }
-    // narrow launches (one pair per thread) keep per-thread inversions: the
-    // block's shared one would add warp 0's group products to their latency
-    const bool share = chunk >= 2;
-    if (!share && count == 0) return;
     // the backward multiplications inlined in both builds of level 0 (n = 2^16,
     // natural build: 131 -> 127 us); the tree's narrow levels keep them called
-    int adds = batch_pairs<S, true>(src, count, inv_kind, share ? sh : nullptr);
+    int adds = batch_pairs<S, true, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh);
     if (stats) warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
 }
 
-template <int S>
+template <int S, int PLACE>
 __global__ void __launch_bounds__(256) k_accum_level0(LEVEL0_PARAMS) {
-    accum_level0<S, false>(LEVEL0_ARGS);
+    accum_level0<S, false, PLACE>(LEVEL0_ARGS);
 }
-template <int S>
+template <int S, int PLACE>
 __global__ void __maxnreg__(80) k_accum_level0_wide(LEVEL0_PARAMS) {
-    accum_level0<S, true>(LEVEL0_ARGS);
+    accum_level0<S, true, PLACE>(LEVEL0_ARGS);
 }
 
 // ------------------------------------------------------- pair lists per level
@@ -224,10 +238,12 @@ struct ListSrc {
     __device__ __forceinline__ void store(int k, const aff& r) { g1::store_aff(items + (size_t)qi[k] * 16, r); }
 };
 
-template <int S, bool WIDE>
+template <int S, bool WIDE, int PLACE>
 __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                           ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
-    const uint32_t cnt = ctl->pair_count[grp][level];
+                                           ctl_t* ctl, int grp, int level, int stats, int inv_kind, uint32_t base) {
+    const uint32_t all = ctl->pair_count[grp][level];
+    if (base >= all) return;  // pairs from `base` on, as in accum_level0
+    const uint32_t cnt = all - base;
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t chunk = min((uint64_t)S, ((uint64_t)cnt + nthreads - 1) / nthreads);
     const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -235,29 +251,38 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     // the block may share one inversion: a block with work keeps all its threads
     if ((uint64_t)blockIdx.x * blockDim.x * chunk >= cnt) return;
     const int count = i0 < cnt ? (int)min(chunk, (uint64_t)cnt - i0) : 0;
+    const bool share = chunk >= 2;  // as in accum_level0
+    if (!share && count == 0) return;
     __shared__ uint32_t sh[8 * 256];
+    extern __shared__ uint32_t pre_sh[];
     ListSrc<S> src;
     src.items = items;
     src.half = 1u << (level - 1);
-    for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
-    const bool share = chunk >= 2;  // as in accum_level0
-    if (!share && count == 0) return;
-    int adds = batch_pairs<S, WIDE>(src, count, inv_kind, share ? sh : nullptr);
+    const uint32_t* lst = list + base;
+    if constexpr (PLACE == PLACE_REGS) {
+#pragma unroll
+        for (int k = 0; k < S; k++) src.qi[k] = k < count ? lst[i0 + k] : 0u;
+    } else {
+        for (int k = 0; k < count; k++) src.qi[k] = lst[i0 + k];
+    }
+    int adds = batch_pairs<S, WIDE, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh);
     if (stats) {
         warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
     }
 }
 
-template <int S>
+template <int S, int PLACE>
 __global__ void __launch_bounds__(256) k_accum_list(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                    ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
-    accum_list<S, false>(items, list, ctl, grp, level, stats, inv_kind);
+                                                    ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                                                    uint32_t base) {
+    accum_list<S, false, PLACE>(items, list, ctl, grp, level, stats, inv_kind, base);
 }
-template <int S>
+template <int S, int PLACE>
 __global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, const uint32_t* __restrict__ list,
-                                                  ctl_t* ctl, int grp, int level, int stats, int inv_kind) {
-    accum_list<S, true>(items, list, ctl, grp, level, stats, inv_kind);
+                                                  ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                                                  uint32_t base) {
+    accum_list<S, true, PLACE>(items, list, ctl, grp, level, stats, inv_kind, base);
 }
 
 // ------------------------------------------------------------ small buckets
@@ -323,46 +348,121 @@ static bool wide(uint64_t work, int S, const Resident& res, int per) {
 // waves for small launches, a larger cap never adds a wave; it only halves the
 // inversions of the launches that have more than 32 units per resident thread
 // (a cap of 32 was 4 % slower at n = 2^20 and 6 % at 2^22).
-static int auto_batch(int batch_s, uint64_t, const Resident&) { return batch_s ? batch_s : 64; }
+static int auto_batch(int batch_s) { return batch_s ? batch_s : 64; }
 
-template <int S>
-static void level0_t(int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi, uint32_t nsplit,
-                     const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t* items,
-                     ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
-    if (wide(units_ub, S, res, 32))
-        k_accum_level0_wide<S><<<grid_for(units_ub, S, tpb, res.wide), tpb, 0, st>>>(
-            points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
-    else
-        k_accum_level0<S><<<grid_for(units_ub, S, tpb, res.narrow), tpb, 0, st>>>(
-            points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
-}
+// Prefix products in shared memory take S x 32 bytes per thread; a block may
+// use at most this much for them (the rest of the SM's 228 KB holds the
+// block-inversion buffer and at least one more block's static use).
+constexpr int kPreSharedMax = 200 << 10;
 
-template <int S>
-static void list_t(int tpb, const Resident& res, uint32_t* items, const uint32_t* list, ctl_t* ctl, uint64_t cap,
-                   int grp, int level, int stats, int inv_kind, cudaStream_t st) {
-    if (wide(cap, S, res, 8))
-        k_accum_list_wide<S><<<grid_for(cap, S, tpb, res.wide), tpb, 0, st>>>(items, list, ctl, grp, level, stats,
-                                                                              inv_kind);
-    else
-        k_accum_list<S><<<grid_for(cap, S, tpb, res.narrow), tpb, 0, st>>>(items, list, ctl, grp, level, stats,
-                                                                          inv_kind);
-}
-
-void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi,
-                         uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
-#define L0(S) \
-    level0_t<S>(tpb, res, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, units_ub, stats, inv_kind, st)
-    switch (auto_batch(batch_s, units_ub, res)) {
-        case 1: L0(1); break;
-        case 2: L0(2); break;
-        case 4: L0(4); break;
-        case 8: L0(8); break;
-        case 16: L0(16); break;
-        case 64: L0(64); break;
-        default: L0(32); break;
+// The batch size a placement runs with: the request (automatic = 64), clamped
+// to the instantiated sizes -- PLACE_LOCAL 1..64, PLACE_SHARED 4..32 and
+// S x 32 x tpb within kPreSharedMax, PLACE_REGS 2..8.
+int placed_batch(int batch_s, int place, int tpb) {
+    int S = auto_batch(batch_s);
+    if (place == PLACE_SHARED) {
+        S = std::max(4, std::min(S, 32));
+        while (S > 4 && S * 32 * tpb > kPreSharedMax) S >>= 1;
+    } else if (place == PLACE_REGS) {
+        S = std::max(2, std::min(S, 8));
     }
+    return S;
+}
+
+// One accumulation step: the natural or the register-capped build of the
+// placement's kernel over `work` units (an upper bound; the kernels read the
+// exact count on the device), with a grid from grid_for and dynamic shared
+// memory for PLACE_SHARED (whose resident threads follow from that memory).
+// A grid cap (MSM_G1_PARAM_GRID) below that grid splits the work into
+// consecutive launches of cap x tpb x S units each, the kernel's last
+// argument giving each launch's first unit.
+template <class KN, class KW, class... Args>
+static int launch_placed(KN kn, KW kw, int place, int S, int per, int tpb, const Resident& res, uint64_t work,
+                          int grid_cap, cudaStream_t st, Args... args) {
+    const size_t dyn = place == PLACE_SHARED ? (size_t)S * 32 * tpb : 0;
+    Resident r = res;
+    if (place == PLACE_SHARED) {
+        int dev = 0, sms = 0, bn = 0, bw = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bn, kn, tpb, dyn);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bw, kw, tpb, dyn);
+        r.narrow = (uint64_t)sms * std::max(1, bn) * tpb;
+        r.wide = (uint64_t)sms * std::max(1, bw) * tpb;
+    }
+    // register-resident prefix products have no capped build: the cap would spill them
+    const bool use_wide = place != PLACE_REGS && wide(work, S, r, per);
+    const unsigned blocks = grid_for(work, S, tpb, use_wide ? r.wide : r.narrow);
+    if (grid_cap <= 0 || blocks <= (unsigned)grid_cap) {
+        if (use_wide) kw<<<blocks, tpb, dyn, st>>>(args..., 0u);
+        else kn<<<blocks, tpb, dyn, st>>>(args..., 0u);
+        return 1;
+    }
+    const uint64_t per_launch = (uint64_t)grid_cap * tpb * S;
+    int launches = 0;
+    for (uint64_t base = 0; base < work; base += per_launch, launches++) {
+        if (use_wide) kw<<<grid_cap, tpb, dyn, st>>>(args..., (uint32_t)base);
+        else kn<<<grid_cap, tpb, dyn, st>>>(args..., (uint32_t)base);
+    }
+    return launches;
+}
+
+template <int S, int PLACE>
+static int level0_t(int tpb, const Resident& res, int grid_cap, const uint32_t* points, const uint32_t* phi,
+                     uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
+                     uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
+    return launch_placed(k_accum_level0<S, PLACE>, k_accum_level0_wide<S, PLACE>, PLACE, S, 32, tpb, res, units_ub,
+                  grid_cap, st, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, stats, inv_kind);
+}
+
+template <int S, int PLACE>
+static int list_t(int tpb, const Resident& res, int grid_cap, uint32_t* items, const uint32_t* list, ctl_t* ctl,
+                   uint64_t cap, int grp, int level, int stats, int inv_kind, cudaStream_t st) {
+    return launch_placed(k_accum_list<S, PLACE>, k_accum_list_wide<S, PLACE>, PLACE, S, 8, tpb, res, cap, grid_cap, st,
+                  items, list, ctl, grp, level, stats, inv_kind);
+}
+
+// Dispatch on (placement, batch size) to the instantiated kernels.
+#define ACCUM_DISPATCH(F)                               \
+    switch (place) {                                    \
+        case PLACE_SHARED:                              \
+            switch (S) {                                \
+                case 4: F(4, PLACE_SHARED); break;      \
+                case 8: F(8, PLACE_SHARED); break;      \
+                case 16: F(16, PLACE_SHARED); break;    \
+                default: F(32, PLACE_SHARED); break;    \
+            }                                           \
+            break;                                      \
+        case PLACE_REGS:                                \
+            switch (S) {                                \
+                case 2: F(2, PLACE_REGS); break;        \
+                case 4: F(4, PLACE_REGS); break;        \
+                default: F(8, PLACE_REGS); break;       \
+            }                                           \
+            break;                                      \
+        default:                                        \
+            switch (S) {                                \
+                case 1: F(1, PLACE_LOCAL); break;       \
+                case 2: F(2, PLACE_LOCAL); break;       \
+                case 4: F(4, PLACE_LOCAL); break;       \
+                case 8: F(8, PLACE_LOCAL); break;       \
+                case 16: F(16, PLACE_LOCAL); break;     \
+                case 32: F(32, PLACE_LOCAL); break;     \
+                default: F(64, PLACE_LOCAL); break;     \
+            }                                           \
+    }
+
+int launch_accum_level0(const AccumKnobs& kb, const Resident& res, const uint32_t* points, const uint32_t* phi,
+                        uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
+                        uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st) {
+    const int place = kb.place, S = placed_batch(kb.batch_s, kb.place, kb.tpb);
+    int launches = 0;
+#define L0(SS, PP)                                                                                              \
+    launches = level0_t<SS, PP>(kb.tpb, res, kb.grid, points, phi, nsplit, entries, offsets, g0, g1, items, ctl, \
+                                units_ub, stats, inv_kind, st)
+    ACCUM_DISPATCH(L0)
 #undef L0
+    return launches;
 }
 
 void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
@@ -370,23 +470,43 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
     k_build_pairs<<<(nb + 255) / 256, 256, 0, st>>>(offsets, nb, pairs, lay, ctl);
 }
 
-void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
-                        cudaStream_t st) {
+int launch_accum_level(const AccumKnobs& kb, const Resident& res, uint32_t* items, const uint32_t* pairs,
+                       const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                       cudaStream_t st) {
     const uint32_t* list = pairs + lay.base[grp][level];
     uint64_t cap = lay.cap[grp][level];
-#define LV(S) list_t<S>(tpb, res, items, list, ctl, cap, grp, level, stats, inv_kind, st)
-    switch (auto_batch(batch_s, cap, res)) {
-        case 1: LV(1); break;
-        case 2: LV(2); break;
-        case 4: LV(4); break;
-        case 8: LV(8); break;
-        case 16: LV(16); break;
-        case 64: LV(64); break;
-        default: LV(32); break;
-    }
+    const int place = kb.place, S = placed_batch(kb.batch_s, kb.place, kb.tpb);
+    int launches = 0;
+#define LV(SS, PP) \
+    launches = list_t<SS, PP>(kb.tpb, res, kb.grid, items, list, ctl, cap, grp, level, stats, inv_kind, st)
+    ACCUM_DISPATCH(LV)
 #undef LV
+    return launches;
 }
+
+// The shared-memory placement's kernels may take up to kPreSharedMax bytes of
+// dynamic shared memory; returns false if the device refuses.
+static bool set_shared_limit() {
+    bool ok = true;
+#define SETMAX(SS, PP)                                                                                             \
+    ok = ok && cudaFuncSetAttribute(k_accum_level0<SS, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,          \
+                                    kPreSharedMax) == cudaSuccess;                                              \
+    ok = ok && cudaFuncSetAttribute(k_accum_level0_wide<SS, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                    kPreSharedMax) == cudaSuccess;                                              \
+    ok = ok && cudaFuncSetAttribute(k_accum_list<SS, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
+                                    kPreSharedMax) == cudaSuccess;                                              \
+    ok = ok && cudaFuncSetAttribute(k_accum_list_wide<SS, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
+                                    kPreSharedMax) == cudaSuccess;
+    SETMAX(4, PLACE_SHARED)
+    SETMAX(8, PLACE_SHARED)
+    SETMAX(16, PLACE_SHARED)
+    SETMAX(32, PLACE_SHARED)
+#undef SETMAX
+    cudaGetLastError();
+    return ok;
+}
+
+bool accum_prepare_device() { return set_shared_limit(); }
 
 }  // namespace msm
 
@@ -396,10 +516,10 @@ Resident accum_resident_threads(int tpb) {
     int dev = 0, sms = 0, b0 = 0, b1 = 0, w0 = 0, w1 = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_accum_level0<32>, tpb, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_accum_list<32>, tpb, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w0, k_accum_level0_wide<32>, tpb, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w1, k_accum_list_wide<32>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_accum_level0<32, PLACE_LOCAL>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_accum_list<32, PLACE_LOCAL>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w0, k_accum_level0_wide<32, PLACE_LOCAL>, tpb, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w1, k_accum_list_wide<32, PLACE_LOCAL>, tpb, 0);
     Resident r;
     r.narrow = (uint64_t)sms * (uint64_t)std::max(1, std::min(b0, b1)) * (uint64_t)tpb;
     r.wide = (uint64_t)sms * (uint64_t)std::max(1, std::min(w0, w1)) * (uint64_t)tpb;

@@ -247,15 +247,50 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
     return v;
 }
 
+// Where a batch keeps its prefix products (the pages' pref_scratch, which they
+// move between private and workgroup memory: PR #23738 "stream-walker S-sweep",
+// section "What would actually win"):
+//  * PLACE_LOCAL: an array in the thread's stack frame.  Its dynamic index puts
+//    it in local memory -- device memory (HBM) private to the thread, cached
+//    in L1 and L2 -- so this is the HBM-scratch placement; the default.
+//  * PLACE_SHARED: the block's dynamic shared memory, word w of product k of
+//    thread i at pre[(8 k + w) blockDim.x + i] (consecutive lanes hit
+//    consecutive banks); S x 32 bytes per thread.
+//  * PLACE_REGS: registers -- both loops fully unrolled so every index is a
+//    constant (small S only: S x 8 registers, and S copies of the loop body).
+constexpr int PLACE_LOCAL = 0;
+constexpr int PLACE_SHARED = 1;
+constexpr int PLACE_REGS = 2;
+
+template <int S, int PLACE>
+struct PreStore {
+    fe v[S];
+    __device__ __forceinline__ void set(int k, const fe& a) { v[k] = a; }
+    __device__ __forceinline__ fe get(int k) const { return v[k]; }
+};
+template <int S>
+struct PreStore<S, PLACE_SHARED> {
+    uint32_t* base;
+    __device__ __forceinline__ void set(int k, const fe& a) {
+#pragma unroll
+        for (int w = 0; w < 8; w++) base[(8 * k + w) * blockDim.x + threadIdx.x] = a.v[w];
+    }
+    __device__ __forceinline__ fe get(int k) const {
+        fe a;
+#pragma unroll
+        for (int w = 0; w < 8; w++) a.v[w] = base[(8 * k + w) * blockDim.x + threadIdx.x];
+        return a;
+    }
+};
+
 // Run one batch of up to S pair additions.  Src supplies, per slot k < count:
 //   bool has_q(k); fe xp(k), xq(k); void ys(k, fe& yp, fe& yq);
 //   aff p(k), q(k); void store(k, const aff&).
 // Returns the number of slots that were true additions (ADD or DBL).
 //
-// The per-slot loops stay rolled: unrolled, S copies of the inlined
-// multiplications overflow the instruction cache (the kernel then stalls on
-// instruction fetch) and pin S x 8 registers of prefix products.  The prefix
-// products live in thread-local memory.  The multiplications of Montgomery's
+// Except with PLACE_REGS the per-slot loops stay rolled: unrolled, S copies of
+// the inlined multiplications overflow the instruction cache (the kernel then
+// stalls on instruction fetch) and pin S x 8 registers of prefix products.  The multiplications of Montgomery's
 // trick are inlined -- the forward one always, the two backward ones when
 // INLINE_BACK -- the others are called: inlined, a multiplication needs no
 // moves into and out of the call's argument registers (which occupy the same
@@ -276,14 +311,16 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
 // NOT done").
 // With sh (shared scratch of 8 x blockDim.x words) the block's threads share
 // one inversion (block_inverse): then every thread of the block must call,
-// those without pairs with count = 0.
-template <int S, bool INLINE_BACK, class Src>
-__device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0, uint32_t* sh = nullptr) {
-    fe pre[S];
+// those without pairs with count = 0.  pre_sh is the block's prefix-product
+// area for PLACE_SHARED (S x 8 x blockDim.x words), unused otherwise.
+template <int S, bool INLINE_BACK, int PLACE = PLACE_LOCAL, class Src>
+__device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0, uint32_t* sh = nullptr,
+                                           uint32_t* pre_sh = nullptr) {
+    PreStore<S, PLACE> pre;
+    if constexpr (PLACE == PLACE_SHARED) pre.base = pre_sh;
     fe acc = fq::one();
     int adds = 0;
-#pragma unroll 1
-    for (int k = 0; k < count; k++) {
+    auto forward = [&](int k) {
         bool hq = src.has_q(k);
         fe xp = src.xp(k);
         fe xq = hq ? src.xq(k) : fq::zero();
@@ -292,11 +329,18 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
         fe d = pair_denominator(cs, xp, xq, yp);
         adds += (cs == PC_ADD || cs == PC_DBL);
         acc = (k == 0) ? d : fq::mul_lazy_inline(acc, d);
-        pre[k] = acc;
+        pre.set(k, acc);
+    };
+    if constexpr (PLACE == PLACE_REGS) {
+#pragma unroll
+        for (int k = 0; k < S; k++)
+            if (k < count) forward(k);
+    } else {
+#pragma unroll 1
+        for (int k = 0; k < count; k++) forward(k);
     }
     fe inv = sh ? block_inverse(acc, sh, inv_kind) : inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
-#pragma unroll 1
-    for (int k = count - 1; k >= 0; k--) {
+    auto backward = [&](int k) {
         aff p = src.p(k);
         bool hq = src.has_q(k);
         aff q = hq ? src.q(k) : g1::aff_inf();
@@ -306,14 +350,22 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
         fe dinv = inv;
         if (k > 0) {
             if (INLINE_BACK) {
-                dinv = fq::mul_lazy_inline(inv, pre[k - 1]);
+                dinv = fq::mul_lazy_inline(inv, pre.get(k - 1));
                 inv = fq::mul_lazy_inline(inv, d);
             } else {
-                dinv = fq::mul_lazy(inv, pre[k - 1]);
+                dinv = fq::mul_lazy(inv, pre.get(k - 1));
                 inv = fq::mul_lazy(inv, d);
             }
         }
         src.store(k, pair_result(cs, p, q, dinv));
+    };
+    if constexpr (PLACE == PLACE_REGS) {
+#pragma unroll
+        for (int j = 0; j < S; j++)
+            if (S - 1 - j < count) backward(S - 1 - j);
+    } else {
+#pragma unroll 1
+        for (int k = count - 1; k >= 0; k--) backward(k);
     }
     return adds;
 }

@@ -634,6 +634,7 @@ struct msm_g1_ctx {
     int groups;            // window groups of the pipelined schedule (1 = serial)
     bool streams_ok;       // the context's own streams and events exist
     bool slice_sort_ok;    // the shared-memory sort kernels may take 128 KB of shared memory
+    bool shared_place_ok;  // the accumulation kernels may keep prefix products in shared memory
     // graph replay of small MSMs: the last captured run and its arguments
     int graph_on;                 // MSM_G1_PARAM_GRAPH
     cudaStream_t cap_stream;      // where runs are captured and replayed
@@ -652,6 +653,8 @@ struct msm_g1_ctx {
     ctl_t* ctl;
     bool gen_ready;
     int batch_s, tpb, timing, stats;
+    int acc_place;         // MSM_G1_PARAM_ACC_PLACEMENT
+    int grid;              // MSM_G1_PARAM_GRID (0: automatic)
     int last_launches;
     cudaEvent_t ev[kPhases + 1];
     bool events_made;
@@ -972,6 +975,7 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
             cudaFuncSetAttribute(k_hist_slices, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
             cudaFuncSetAttribute(k_scatter_slices, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
         cudaGetLastError();
+        c->shared_place_ok = accum_prepare_device();
     }
     *out = c;
     return MSM_G1_OK;
@@ -1053,6 +1057,16 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             if (value != 0 && value != 1) return MSM_G1_ERR_INVALID_ARG;
             c->graph_on = value;
             return MSM_G1_OK;
+        case MSM_G1_PARAM_GRID:
+            if (value < 0) return MSM_G1_ERR_INVALID_ARG;
+            c->grid = value;
+            return MSM_G1_OK;
+        case MSM_G1_PARAM_ACC_PLACEMENT:
+            if (value != MSM_G1_ACC_LOCAL && value != MSM_G1_ACC_SHARED && value != MSM_G1_ACC_REGISTERS)
+                return MSM_G1_ERR_INVALID_ARG;
+            if (value == MSM_G1_ACC_SHARED && !c->shared_place_ok) return MSM_G1_ERR_INVALID_ARG;
+            c->acc_place = value;
+            return MSM_G1_OK;
         default:
             return MSM_G1_ERR_INVALID_ARG;
     }
@@ -1070,6 +1084,8 @@ int msm_g1_get_param(const msm_g1_ctx* c, int key, int* value) {
         case MSM_G1_PARAM_GLV: *value = c->glv; return MSM_G1_OK;
         case MSM_G1_PARAM_INVERSION: *value = c->inv_kind; return MSM_G1_OK;
         case MSM_G1_PARAM_GRAPH: *value = c->graph_on; return MSM_G1_OK;
+        case MSM_G1_PARAM_GRID: *value = c->grid; return MSM_G1_OK;
+        case MSM_G1_PARAM_ACC_PLACEMENT: *value = c->acc_place; return MSM_G1_OK;
         default: return MSM_G1_ERR_INVALID_ARG;
     }
 }
@@ -1212,6 +1228,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     const ReducePlan rp = reduce_plan(B);
     const uint32_t L = rp.L, G = rp.G;
     if (rp.jobs > MAX_REDUCE_JOBS) return MSM_G1_ERR_INVALID_ARG;  // unreachable for c <= 20
+    const AccumKnobs knobs{c->batch_s, c->tpb, c->acc_place, c->grid};
     c->last_finish_t = lay.finish_t;
     c->last_chunk_len = L;
     c->last_groups = (uint32_t)lay.groups;
@@ -1219,17 +1236,15 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     auto level0 = [&](int j, cudaStream_t s) {
         if (side) cudaStreamWaitEvent(s, c->ev_points, 0);
         const int nw = lay.w_hi[j] - lay.w_lo[j];
-        launch_accum_level0(c->batch_s, c->tpb, resident, points, c->phi, nsplit, c->entries, c->offsets,
-                            (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
-                            (terms_pw * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
-        launches++;
+        launches += launch_accum_level0(knobs, resident, points, c->phi, nsplit, c->entries, c->offsets,
+                                        (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
+                                        (terms_pw * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
     };
     auto tree = [&](int j, cudaStream_t s) {
         // levels while some bucket may still hold two items: 2^level < max bucket <= terms
         for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < terms; level++) {
-            launch_accum_level(c->batch_s, c->tpb, resident, c->items, c->pairs, lay, c->ctl, j, level, stats,
-                               c->inv_kind, s);
-            launches++;
+            launches += launch_accum_level(knobs, resident, c->items, c->pairs, lay, c->ctl, j, level, stats,
+                                           c->inv_kind, s);
         }
     };
     auto reduce = [&](int j, cudaStream_t s) {

@@ -43,21 +43,33 @@ struct Resident {
     uint64_t narrow, wide;
 };
 
-// accumulation launchers (msm_accum.cu); batch_s in {1, 2, 4, 8, 16, 32, 64} (0: chosen
-// per launch) is the
-// largest number of pairs a thread shares one inversion across
+// The accumulation knobs: batch_s in {1, 2, 4, 8, 16, 32, 64} (0: automatic)
+// is the largest number of pairs a thread shares one inversion across; tpb
+// the threads per block; place where a batch keeps its prefix products
+// (PLACE_LOCAL, PLACE_SHARED, PLACE_REGS in msm_core.cuh); grid the most
+// blocks a launch may use (0: automatic).
+struct AccumKnobs {
+    int batch_s, tpb, place, grid;
+};
+
+// accumulation launchers (msm_accum.cu):
 // level 0 over the units of buckets [g0, g1); levels >= 1 over group grp's list;
 // inv_kind: 0 = safegcd, 1 = Fermat
-// (entry indices below nsplit address points, the others phi - nsplit)
-void launch_accum_level0(int batch_s, int tpb, const Resident& res, const uint32_t* points, const uint32_t* phi,
-                         uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
-                         uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st);
+// (entry indices below nsplit address points, the others phi - nsplit);
+// each returns the number of kernels it launched
+int launch_accum_level0(const AccumKnobs& kb, const Resident& res, const uint32_t* points, const uint32_t* phi,
+                        uint32_t nsplit, const uint32_t* entries, const uint32_t* offsets, uint32_t g0, uint32_t g1,
+                        uint32_t* items, ctl_t* ctl, uint64_t units_ub, int stats, int inv_kind, cudaStream_t st);
 void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, const PairLayout& lay, ctl_t* ctl,
                         cudaStream_t st);
-void launch_accum_level(int batch_s, int tpb, const Resident& res, uint32_t* items, const uint32_t* pairs,
-                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
-                        cudaStream_t st);
+int launch_accum_level(const AccumKnobs& kb, const Resident& res, uint32_t* items, const uint32_t* pairs,
+                       const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
+                       cudaStream_t st);
 Resident accum_resident_threads(int tpb);
+// the batch size a launch with these knobs runs with
+int placed_batch(int batch_s, int place, int tpb);
+// per-device set-up of the accumulation kernels (shared-memory limits); false on failure
+bool accum_prepare_device();
 // Jacobian sums of the buckets of [g0, g1) that left the tree with >= 2 items
 void launch_finish(const uint32_t* items, const uint32_t* offsets, uint32_t g0, uint32_t g1, uint32_t finish_t,
                    uint32_t* jsum, uint64_t resident, cudaStream_t st);

@@ -35,6 +35,11 @@ PARAM_FINISH = 6
 PARAM_GLV = 7
 PARAM_INVERSION = 8
 PARAM_GRAPH = 9
+PARAM_GRID = 10
+PARAM_ACC_PLACEMENT = 11
+ACC_LOCAL = 0
+ACC_SHARED = 1
+ACC_REGISTERS = 2
 PLAIN_BITS = 255  # bits the signed windows of a scalar mod r cover
 GLV_BITS = 128    # bits the signed windows of one GLV half cover
 

@@ -61,8 +61,10 @@ extern "C" {
 
 /* Tunable keys for msm_g1_set_param / msm_g1_get_param. */
 #define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32, 64,
-                                  or 0 = automatic (default, 64) */
-#define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128) */
+                                  or 0 = automatic (default, 64).  The pages' walkerS, additions per inversion
+                                  (PR #23738 "stream-walker S-sweep", section "What landed here") */
+#define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128).
+                                  The pages' walkerTpb (same section) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
 #define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = automatic
@@ -77,6 +79,20 @@ extern "C" {
                                   a CUDA graph on the context's own stream and replays it while the pointers,
                                   n, window_c and the parameters stay the same (setting any parameter drops
                                   the graph); 0: every run launches its kernels directly */
+#define MSM_G1_PARAM_GRID 10   /* most blocks one accumulation launch may use (level 0 and every tree level):
+                                  0 = automatic (default: whole resident waves for launches of fewer than four
+                                  waves, else one block per tpb x S additions); a smaller cap makes each thread
+                                  take several batches in turn.  The pages' walkerMaxWg, the cap on the
+                                  walker's workgroups (PR #23738 "stream-walker S-sweep", section "What landed
+                                  here") */
+#define MSM_G1_PARAM_ACC_PLACEMENT 11 /* where a batch keeps its S prefix products (the pages' pref_scratch,
+                                  PR #23738, section "What would actually win"): MSM_G1_ACC_LOCAL (default),
+                                  MSM_G1_ACC_SHARED or MSM_G1_ACC_REGISTERS (values below).  The placement
+                                  bounds the batch size: shared 4..32 with S x 32 x TPB <= 200 KB, registers
+                                  2..8; a request outside is clamped into that range */
+#define MSM_G1_ACC_LOCAL 0     /* the thread's stack frame: device memory (HBM) cached in L1 and L2 */
+#define MSM_G1_ACC_SHARED 1    /* the block's shared memory, S x 32 bytes per thread */
+#define MSM_G1_ACC_REGISTERS 2 /* registers: the batch's loops unrolled so that every index is constant */
 
 typedef struct msm_g1_ctx msm_g1_ctx;
 
@@ -158,9 +174,14 @@ int msm_g1_mul_generator(msm_g1_ctx *ctx, const uint32_t *scalars, size_t n, uin
  * The source pages have no counterpart: this entry point exists for such
  * callers only.  No context: all scratch comes from one fixed 8 MiB array in
  * device global memory that the library holds on every GPU that loads it until
- * the process exits.  Limits: n <= 4096 and window_c <= 10 (0 picks a window
- * within that limit); larger n or c returns MSM_G1_ERR_CAPACITY without device
- * work.  The first call on a device looks up the array's device address on
+ * the process exits.  Limits: window_c <= 10.  With window_c in 8..10, or 0
+ * (which picks a window within that range), any n <= 4096 fits.  A smaller
+ * window needs more bucket entries per point (2 ceil(128 / c) with the GLV
+ * split, against a fixed budget of 4096 x 32), so it fits proportionally fewer
+ * points: n <= 3767 at c = 7, for instance.  Inputs beyond the limits return
+ * MSM_G1_ERR_CAPACITY without device work.  The device-side capacity check
+ * that msm_g1_last_stats reports for a context (out[7]) has no reader here;
+ * the fixed sizing keeps it from ever firing.  The first call on a device looks up the array's device address on
  * that device (cudaGetSymbolAddress); make that first call before any stream
  * capture.  Every call reuses the same array: the calls clear what must start
  * at zero themselves, but calls whose device work overlaps (different streams,

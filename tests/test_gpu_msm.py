@@ -30,15 +30,21 @@ def ctx(max_n, max_c):
     return _ctx[key]
 
 
-def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=0, tpb=128, glv=1):
+def run_gpu(points_affine, k, c, max_n=None, max_c=None, batch_s=0, tpb=128, glv=1, place=0, grid=0):
     n = k.shape[0]
     cx = ctx(max_n or max(n, 1), max_c or max(c, 1))
     cx.set_param(gm.PARAM_BATCH_S, batch_s)
     cx.set_param(gm.PARAM_TPB, tpb)
     cx.set_param(gm.PARAM_GLV, glv)
-    out = cx.run(gpu_points(points_affine), gpu_scalars(k), c)
-    res = normalise(out)
-    assert cx.stats()["error"] == 0
+    cx.set_param(gm.PARAM_ACC_PLACEMENT, place)
+    cx.set_param(gm.PARAM_GRID, grid)
+    try:
+        out = cx.run(gpu_points(points_affine), gpu_scalars(k), c)
+        res = normalise(out)
+        assert cx.stats()["error"] == 0
+    finally:
+        cx.set_param(gm.PARAM_ACC_PLACEMENT, 0)
+        cx.set_param(gm.PARAM_GRID, 0)
     return res
 
 
@@ -89,6 +95,56 @@ def test_knobs(mid_case, batch_s, tpb):
     section "Real-hardware results")."""
     pts, k, expect = mid_case
     assert np.array_equal(run_gpu(pts, k, 13, max_n=20000, max_c=13, batch_s=batch_s, tpb=tpb), expect)
+
+
+PLACEMENTS = {"local": 0, "shared": 1, "registers": 2}
+
+
+@pytest.mark.parametrize("place", ["shared", "registers"])
+@pytest.mark.parametrize("batch_s", [0, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("tpb", [64, 128, 256])
+def test_prefix_placements(mid_case, place, batch_s, tpb):
+    """Prefix products in shared memory or in registers (the pages' choice of
+    where pref_scratch lives: PR #23738 "stream-walker S-sweep", section "What
+    would actually win") give the result of the default placement for every
+    batch size and block size; sizes a placement does not hold are clamped."""
+    pts, k, expect = mid_case
+    got = run_gpu(pts, k, 13, max_n=20000, max_c=13, batch_s=batch_s, tpb=tpb, place=PLACEMENTS[place])
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("place", ["local", "shared", "registers"])
+@pytest.mark.parametrize("glv", [1, 0])
+def test_prefix_placements_on_exceptional_pairs(place, glv):
+    """Equal, opposite and infinite operands inside a batch whose prefix
+    products live in each placement."""
+    r, k = synth.adversarial_workload(30000, 1007)
+    pts = points_from_r(r)
+    got = run_gpu(pts, k, 12, max_n=30000, max_c=16, glv=glv, batch_s=8, place=PLACEMENTS[place])
+    assert np.array_equal(got, expect_oracle(pts, k))
+
+
+@pytest.mark.parametrize("grid", [1, 3, 17, 152, 100000])
+@pytest.mark.parametrize("batch_s", [0, 1, 8])
+def test_grid_cap(mid_case, grid, batch_s):
+    """A cap on the accumulation grid (the pages' walkerMaxWg) splits the
+    work into consecutive launches; the result does not change."""
+    pts, k, expect = mid_case
+    got = run_gpu(pts, k, 13, max_n=20000, max_c=13, batch_s=batch_s, grid=grid)
+    assert np.array_equal(got, expect)
+
+
+def test_new_parameters_reject_bad_values():
+    cx = ctx(20000, 13)
+    for key, bad in ((gm.PARAM_GRID, -1), (gm.PARAM_ACC_PLACEMENT, 3), (gm.PARAM_ACC_PLACEMENT, -1)):
+        with pytest.raises(gm.MsmError):
+            cx.set_param(key, bad)
+    cx.set_param(gm.PARAM_GRID, 5)
+    assert cx.get_param(gm.PARAM_GRID) == 5
+    cx.set_param(gm.PARAM_ACC_PLACEMENT, gm.ACC_SHARED)
+    assert cx.get_param(gm.PARAM_ACC_PLACEMENT) == gm.ACC_SHARED
+    cx.set_param(gm.PARAM_GRID, 0)
+    cx.set_param(gm.PARAM_ACC_PLACEMENT, gm.ACC_LOCAL)
 
 
 @pytest.mark.parametrize("groups", [1, 2, 3, 4])
@@ -490,6 +546,34 @@ def test_config3_n2p20_c16(big_points, batch_s):
     _, k = synth.uniform_workload(n, 1003)
     got = run_gpu(pts_all[:n], k, 16, max_n=n, max_c=16, batch_s=batch_s)
     assert np.array_equal(got, oracle.closed_form(r_all[:n], k))
+
+
+@pytest.mark.parametrize("place", ["local", "shared", "registers"])
+@pytest.mark.parametrize("tpb", [64, 128, 256])
+@pytest.mark.parametrize("batch_s", [4, 8, 16, 32, 64])
+def test_config3_sweep(big_points, place, tpb, batch_s):
+    """Every cell of the n = 2^20 sweep over S, threads per block and the
+    prefix-product placement is bit-exact (the closed form)."""
+    r_all, pts_all = big_points
+    n = 1 << 20
+    k = _config3_scalars()
+    got = run_gpu(pts_all[:n], k, 16, max_n=n, max_c=16, batch_s=batch_s, tpb=tpb, place=PLACEMENTS[place])
+    assert np.array_equal(got, _config3_expect(r_all[:n], k))
+
+
+_c3 = {}
+
+
+def _config3_scalars():
+    if "k" not in _c3:
+        _c3["k"] = synth.uniform_workload(1 << 20, 1003)[1]
+    return _c3["k"]
+
+
+def _config3_expect(r, k):
+    if "e" not in _c3:
+        _c3["e"] = oracle.closed_form(r, k)
+    return _c3["e"]
 
 
 @pytest.mark.parametrize("c,glv", [(16, 1), (17, 1), (18, 1), (16, 0)])

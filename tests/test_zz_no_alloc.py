@@ -54,3 +54,12 @@ def test_noalloc_rejects_sizes_beyond_its_limit():
     rc, out = _noalloc(pts[:1], ks[:1], 0)  # auto window within the limit
     assert rc == gm.OK
     assert np.array_equal(normalise(out), oracle.closed_form(r[:1], k[:1]))
+    # a window below 8 bits takes more entries per point: 4096 points no longer fit at c = 7
+    rc, _ = _noalloc(pts[:4096], ks[:4096], 7)
+    assert rc == gm.ERR_CAPACITY
+    rc, out = _noalloc(pts[:3767], ks[:3767], 7)
+    assert rc == gm.OK
+    assert np.array_equal(normalise(out), oracle.closed_form(r[:3767], k[:3767]))
+    rc, out = _noalloc(pts[:500], ks[:500], 4)  # a small window with few points fits
+    assert rc == gm.OK
+    assert np.array_equal(normalise(out), oracle.closed_form(r[:500], k[:500]))
