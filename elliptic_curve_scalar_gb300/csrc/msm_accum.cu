@@ -285,6 +285,44 @@ __global__ void __maxnreg__(80) k_accum_list_wide(uint32_t* __restrict__ items, 
     accum_list<S, true, PLACE>(items, list, ctl, grp, level, stats, inv_kind, base);
 }
 
+// ------------------------------------------------------------ deep levels
+
+// The tree levels past those the host launches one by one: one block works
+// through level `first` and every later level whose list is non-empty, in
+// rounds of blockDim x S pairs, with a barrier between rounds and levels (a
+// level's pairs read the items the previous level wrote).  The host sizes its
+// per-level launches for the bucket sizes uniform data gives, so this launch
+// usually finds its first level empty and returns at once -- one launch
+// instead of one per possible level; an unusually deep bucket (e.g. many
+// equal scalars) is still summed, by this block.
+template <int S>
+__global__ void __launch_bounds__(256) k_accum_deep(uint32_t* __restrict__ items, const uint32_t* __restrict__ pairs,
+                                                    PairLayout lay, ctl_t* ctl, int grp, int first, int stats,
+                                                    int inv_kind) {
+    __shared__ uint32_t sh[8 * 256];
+    int adds = 0, invs = 0;
+    for (int level = first; level < MAX_LEVELS; level++) {
+        const uint32_t cnt = ctl->pair_count[grp][level];
+        if (cnt == 0) break;  // deeper levels are empty too
+        const uint32_t* list = pairs + lay.base[grp][level];
+        const uint32_t chunk = min((uint32_t)S, (cnt + blockDim.x - 1) / blockDim.x);
+        for (uint32_t base = 0; base < cnt; base += blockDim.x * chunk) {
+            const uint32_t i0 = base + threadIdx.x * chunk;
+            const int count = i0 < cnt ? (int)min(chunk, cnt - i0) : 0;
+            ListSrc<S> src;
+            src.items = items;
+            src.half = 1u << (level - 1);
+            for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
+            // every thread of the block takes part in the shared inversion
+            adds += batch_pairs<S, false>(src, count, inv_kind, sh);
+            invs += threadIdx.x < 32;
+            __syncthreads();  // the next round reuses sh; the next level reads these items
+        }
+        if (stats && threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
+    }
+    if (stats) warp_stats(ctl, adds, invs);
+}
+
 // ------------------------------------------------------------ small buckets
 
 // One thread (W = 1) or one group of W lanes (cooperative additions) per bucket:
@@ -482,6 +520,11 @@ int launch_accum_level(const AccumKnobs& kb, const Resident& res, uint32_t* item
     ACCUM_DISPATCH(LV)
 #undef LV
     return launches;
+}
+
+void launch_accum_deep(uint32_t* items, const uint32_t* pairs, const PairLayout& lay, ctl_t* ctl, int grp, int first,
+                       int stats, int inv_kind, cudaStream_t st) {
+    k_accum_deep<16><<<1, 256, 0, st>>>(items, pairs, lay, ctl, grp, first, stats, inv_kind);
 }
 
 // The shared-memory placement's kernels may take up to kPreSharedMax bytes of

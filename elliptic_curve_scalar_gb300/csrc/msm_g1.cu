@@ -29,12 +29,14 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #include <algorithm>
 #include <mutex>
 
 #include "../../include/msm_g1.h"
 #include "g1_coop.cuh"
+#include "g1_rns.cuh"
 #include "msm_internal.cuh"
 
 using fq::fe;
@@ -479,13 +481,32 @@ __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_jobs(const uint32_t* __re
     if (threadIdx.x < 24) partials[((size_t)(w * jobs + job) * parts + part) * 24 + threadIdx.x] = sm[threadIdx.x];
 }
 
-// One block per window, one warp per job: warp q sums its job's partial sums
-// and shifts the result to its weight -- V_t by 2^t L (t + log2 L doublings),
-// the sum of C_j not at all -- so that the bits are weighted in parallel
-// rather than by a sequential Horner pass; a tree over the jobs' values then
-// gives T_w = sum C_j + L sum_t 2^t V_t.
+// One warp per (window, job): the warp sums its job's partial sums and shifts
+// the result to its weight -- V_t by 2^t L (t + log2 L doublings), the sum of
+// C_j not at all -- so that the bits are weighted in parallel rather than by a
+// sequential Horner pass.  The doublings run in the residue number system
+// (g1_rns.cuh): a chain of them is latency-bound, and there a doubling costs
+// three RNS products (about 400 cycles each) instead of three positional ones
+// (about 870).  The shifted value replaces the job's first partial sum.
+__global__ void __launch_bounds__(32) k_reduce_shift(uint32_t* __restrict__ partials, int w_lo, uint32_t jobs,
+                                                     uint32_t parts, uint32_t log2L) {
+    const uint32_t w = (uint32_t)w_lo + blockIdx.x / jobs, q = blockIdx.x % jobs;
+    uint32_t* src = partials + (size_t)(w * jobs + q) * parts * 24;
+    jac acc = g1::load_jac(src);
+    for (uint32_t p = 1; p < parts; p++) acc = g1c::add(acc, g1::load_jac(src + p * 24));
+    const uint32_t shift = q == 0 ? 0 : q - 1 + log2L;
+    if (shift) {
+        const rns::Ctx C = rns::make_ctx();
+        acc = g1r::dbl_n_positional(C, acc, (int)shift);
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) g1::store_jac(src, acc);
+}
+
+// One block per window, one warp per job: a tree over the jobs' shifted
+// values gives T_w = sum C_j + L sum_t 2^t V_t.
 __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uint32_t* __restrict__ partials, int w_lo,
-                                                                       uint32_t jobs, uint32_t parts, uint32_t log2L,
+                                                                       uint32_t jobs, uint32_t parts,
                                                                        uint32_t* __restrict__ wsums) {
     __shared__ uint32_t sm[MAX_REDUCE_JOBS * 24];
     const uint32_t w = (uint32_t)w_lo + blockIdx.x;
@@ -495,15 +516,7 @@ __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uin
     // the tree runs over span = 2^k >= jobs values; the block has one warp per
     // job, so its first threads set the span - jobs padding values to infinity
     if (threadIdx.x < span - jobs) g1::store_jac(sm + (jobs + threadIdx.x) * 24, g1::jac_inf());
-    if (q < jobs) {
-        const uint32_t* src = partials + (size_t)(w * jobs + q) * parts * 24;
-        jac acc = g1::load_jac(src);
-        for (uint32_t p = 1; p < parts; p++) acc = g1c::add(acc, g1::load_jac(src + p * 24));
-        const uint32_t shift = q == 0 ? 0 : q - 1 + log2L;
-        acc = g1c::dbl_n(acc, (int)shift);
-        __syncwarp();
-        if (lane == 0) g1::store_jac(sm + q * 24, acc);
-    }
+    if (q < jobs && lane < 24) sm[q * 24 + lane] = partials[(size_t)(w * jobs + q) * parts * 24 + lane];
     __syncthreads();
     for (uint32_t h = span >> 1; h >= 1; h >>= 1) {
         if (q < h) {
@@ -518,19 +531,23 @@ __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uin
 
 // ---------------------------------------------------------- 7. combination
 
-// One warp: Horner's rule over windows w_hi-1 .. w_lo with warp-cooperative
-// doublings and additions (the chain of about nbits - c doublings is the latency
-// floor of the whole MSM).  The running value is carried between window groups
-// in acc; the first group starts from its top window, the last writes out.
+// One warp: Horner's rule over windows w_hi-1 .. w_lo (the chain of about
+// nbits - c doublings is the latency floor of the whole MSM), run in the
+// residue number system of g1_rns.cuh: three groups of ten lanes compute the
+// three products of each level of a doubling at once, each product a 32-bit
+// product per residue and two short base extensions, about 400 cycles where a
+// positional product is about 870.  The running value is carried between
+// window groups in acc; the first group starts from its top window, the last
+// writes out.
 __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo, Windows L,
                                uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int first, int last) {
     if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    jac q = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
-    for (int w = first ? w_hi - 2 : w_hi - 1; w >= w_lo; w--) {
-        // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
-        q = g1c::dbl_n(q, window_width(L, w));
-        q = g1c::add(q, g1::load_jac(wsums + (size_t)w * 24));
-    }
+    const rns::Ctx C = rns::make_ctx();
+    const jac q0 = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
+    // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
+    const jac q = g1r::horner(
+        C, q0, first ? w_hi - 2 : w_hi - 1, w_lo, [&](int w) { return window_width(L, w); },
+        [&](int w) { return g1::load_jac(wsums + (size_t)w * 24); });
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
 }
 
@@ -542,8 +559,8 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
 // one addition on the critical path.
 __global__ void k_combine_shift(uint32_t* __restrict__ acc, int bits) {
     if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    jac q = g1::load_jac(acc);
-    q = g1c::dbl_n(q, bits);
+    const rns::Ctx C = rns::make_ctx();
+    const jac q = g1r::dbl_n_positional(C, g1::load_jac(acc), bits);
     if (threadIdx.x == 0) g1::store_jac(acc, q);
 }
 
@@ -558,11 +575,10 @@ __global__ void k_combine_join(uint32_t* __restrict__ acc, const uint32_t* __res
 __global__ void k_combine_batch(const uint32_t* __restrict__ wsums, Windows L, uint32_t* __restrict__ out) {
     const uint32_t m = blockIdx.x;
     const uint32_t* ws = wsums + (size_t)m * L.W * 24;
-    jac q = g1::load_jac(ws + (size_t)(L.W - 1) * 24);
-    for (int w = L.W - 2; w >= 0; w--) {
-        q = g1c::dbl_n(q, window_width(L, w));
-        q = g1c::add(q, g1::load_jac(ws + (size_t)w * 24));
-    }
+    const rns::Ctx C = rns::make_ctx();
+    const jac q = g1r::horner(
+        C, g1::load_jac(ws + (size_t)(L.W - 1) * 24), L.W - 2, 0, [&](int w) { return window_width(L, w); },
+        [&](int w) { return g1::load_jac(ws + (size_t)w * 24); });
     if (threadIdx.x == 0) g1::store_jac(out + (size_t)m * 24, q);
 }
 
@@ -729,6 +745,22 @@ static int auto_finish(uint64_t n, int W, uint64_t resident) {
     if (pairs1 >= 8 * resident) return 1;
     if (pairs1 >= 2 * resident) return 8;
     return 16;
+}
+
+// The tree levels worth a launch of their own for terms_pw terms per window
+// over B buckets: a bucket's level-1 item count h is about terms / (2 B) for
+// uniform scalars (Poisson-like), so the largest one is below
+// h_max = h + 6 sqrt(h) + 8, and level l has pairs while
+// ceil(h_max / 2^(l-1)) > T.  Deeper levels are left to the deep-level
+// launch, which normally finds them empty (n = 2^22: 9 levels instead of 22
+// per window group).
+static int dense_levels(uint64_t terms_pw, uint32_t B, uint32_t finish_t) {
+    const double h = (double)terms_pw / (2.0 * (double)B);
+    const double hmax = h + 6.0 * sqrt(h) + 8.0;
+    const double t = finish_t > 1 ? (double)finish_t : 1.0;
+    int l = 1;
+    while (l < MAX_LEVELS && hmax / (double)(1ull << (l - 1)) > t) l++;
+    return l - 1 < 1 ? 1 : l - 1;
 }
 
 // Window groups (top windows first) and their pair-list layout.
@@ -1240,11 +1272,19 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
                                         (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, c->items, c->ctl,
                                         (terms_pw * nw + (uint64_t)nw * B + 1) / 2, stats, c->inv_kind, s);
     };
+    // Tree levels launched one by one: those uniform data fills (dense_levels);
+    // the rest, usually empty, go to one deep-level launch.
+    const int dense = dense_levels(terms_pw, B, lay.finish_t);
     auto tree = [&](int j, cudaStream_t s) {
         // levels while some bucket may still hold two items: 2^level < max bucket <= terms
-        for (int level = 1; level < MAX_LEVELS && ((uint64_t)1 << level) < terms; level++) {
+        int level = 1;
+        for (; level <= dense && level < MAX_LEVELS && ((uint64_t)1 << level) < terms; level++) {
             launches += launch_accum_level(knobs, resident, c->items, c->pairs, lay, c->ctl, j, level, stats,
                                            c->inv_kind, s);
+        }
+        if (level < MAX_LEVELS && ((uint64_t)1 << level) < terms) {
+            launch_accum_deep(c->items, c->pairs, lay, c->ctl, j, level, stats, c->inv_kind, s);
+            launches++;
         }
     };
     auto reduce = [&](int j, cudaStream_t s) {
@@ -1266,8 +1306,9 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
                                                                     lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
         k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, rp.tpb, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
                                                                           rp.parts, rp.m, c->partials);
-        k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L), c->wsums);
-        launches += 3;
+        k_reduce_shift<<<(unsigned)nw * rp.jobs, 32, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L));
+        k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, c->wsums);
+        launches += 4;
     };
     auto combine = [&](int j, cudaStream_t s) {
         if (count > 1)  // one warp per MSM of the batch

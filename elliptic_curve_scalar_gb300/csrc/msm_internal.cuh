@@ -65,6 +65,9 @@ void launch_build_pairs(const uint32_t* offsets, uint32_t nb, uint32_t* pairs, c
 int launch_accum_level(const AccumKnobs& kb, const Resident& res, uint32_t* items, const uint32_t* pairs,
                        const PairLayout& lay, ctl_t* ctl, int grp, int level, int stats, int inv_kind,
                        cudaStream_t st);
+// one block over tree levels first, first + 1, ... of group grp while their lists are non-empty
+void launch_accum_deep(uint32_t* items, const uint32_t* pairs, const PairLayout& lay, ctl_t* ctl, int grp, int first,
+                       int stats, int inv_kind, cudaStream_t st);
 Resident accum_resident_threads(int tpb);
 // the batch size a launch with these knobs runs with
 int placed_batch(int batch_s, int place, int tpb);

@@ -77,6 +77,7 @@ _SIGS = {
     "msm_g1_test_batch_add": (_i, [_vp, _vp, _vp, _sz, _i, _i, _vp]),
     "msm_g1_test_digits": (_i, [_vp, _sz, _i, _i, _vp, _vp]),
     "msm_g1_test_glv_split": (_i, [_vp, _sz, _vp, _vp]),
+    "msm_g1_test_rns": (_i, [_i, _vp, _vp, _vp, _sz, _i, _vp]),
     "msm_g1_glv_constants": (_i, [_vp, _vp]),
     "msm_g1_debug_read": (_i, [_vp, _i, _vp, _sz, ctypes.POINTER(_sz)]),
 }

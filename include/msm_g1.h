@@ -83,10 +83,12 @@ extern "C" {
                                   0 = automatic (default: whole resident waves for launches of fewer than four
                                   waves, else one block per tpb x S additions); a smaller cap makes each thread
                                   take several batches in turn.  The pages' walkerMaxWg, the cap on the
-                                  walker's workgroups (PR #23738 "stream-walker S-sweep", section "What landed
-                                  here") */
+                                  walker's workgroups (PR #23736 "stream-walker -- amortize the field inversion
+                                  via large S + private pref_scratch", section "Change (correct, landed)") */
 #define MSM_G1_PARAM_ACC_PLACEMENT 11 /* where a batch keeps its S prefix products (the pages' pref_scratch,
-                                  PR #23738, section "What would actually win"): MSM_G1_ACC_LOCAL (default),
+                                  moved from workgroup to private memory in PR #23736, section "Change
+                                  (correct, landed)"; PR #23738 "stream-walker S-sweep", section "What would
+                                  actually win", asks to move it out again): MSM_G1_ACC_LOCAL (default),
                                   MSM_G1_ACC_SHARED or MSM_G1_ACC_REGISTERS (values below).  The placement
                                   bounds the batch size: shared 4..32 with S x 32 x TPB <= 200 KB, registers
                                   2..8; a request outside is clamped into that range */
@@ -97,7 +99,9 @@ extern "C" {
 typedef struct msm_g1_ctx msm_g1_ctx;
 
 /* Create a context on the current CUDA device and allocate its device
- * scratch (one allocation, owned by the context).  Scratch covers every run
+ * scratch (one allocation, owned by the context): the buffers the pages size
+ * per configuration (PR #23738 "stream-walker S-sweep", section "What landed
+ * here": "all S-dependent buffer sizing"), sized here once for the largest run.  Scratch covers every run
  * with n <= max_n and c <= max_c whose entry count (n * ceil(255/c) plain,
  * 2n * ceil(128/c) with the GLV split) is at most
  * max_n * max(ceil(255/c8), 2 ceil(128/c8)), c8 = min(8, max_c); every c >= c8
@@ -107,14 +111,16 @@ typedef struct msm_g1_ctx msm_g1_ctx;
  * allocation fails.  On error *ctx is set to NULL. */
 int msm_g1_create(msm_g1_ctx **ctx, size_t max_n, int max_c);
 
-/* As msm_g1_create, with the per-bucket and per-window buffers sized for
+/* No page counterpart (the pages run one MSM at a time).
+ * As msm_g1_create, with the per-bucket and per-window buffers sized for
  * max_batch MSMs fused in one pass of msm_g1_run_batch (1 <= max_batch <=
  * 4096); max_n then bounds the terms of a whole pass.  msm_g1_create(ctx, n,
  * c) is msm_g1_create_batch(ctx, n, c, 1); a batch that does not fit one pass
  * runs as several. */
 int msm_g1_create_batch(msm_g1_ctx **ctx, size_t max_n, int max_c, int max_batch);
 
-/* Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
+/* The MSM the pages accelerate (see the file comment for its steps and sources).
+ * Q = sum_{i<n} k_i * P_i, written to out_jacobian (device, 24 uint32).
  * With MSM_G1_PARAM_GLV = 1 (the default) each term is split by the
  * endomorphism phi(x, y) = (beta x, y) = [lambda](x, y) of BN254 G1 into
  * k1 P + k2 phi(P) with |k1|, |k2| < 2^127 (Gallant-Lambert-Vanstone), so the
@@ -133,7 +139,8 @@ int msm_g1_create_batch(msm_g1_ctx **ctx, size_t max_n, int max_c, int max_batch
 int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
                int window_c, uint32_t *out_jacobian, cudaStream_t stream);
 
-/* A batch of count independent MSMs: out_jacobian[m] (24 uint32 each,
+/* No page counterpart: many MSMs fused into one pass.
+ * A batch of count independent MSMs: out_jacobian[m] (24 uint32 each,
  * device) = sum over terms i in [offsets[m], offsets[m+1]) of k_i * P_i.
  * points_affine / scalars: device, the MSMs' terms concatenated (offsets[count]
  * terms, layouts as for msm_g1_run); offsets: HOST array of count + 1
@@ -147,7 +154,9 @@ int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *s
 int msm_g1_run_batch(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, const size_t *offsets,
                      int count, int window_c, uint32_t *out_jacobian, cudaStream_t stream);
 
-/* The same MSM with inputs and output in HOST memory: points_affine (n x 16
+/* The pages' "wall" time covers the whole call from the host (PR #23738,
+ * section "Real-hardware data"); this entry point is that call.
+ * The same MSM with inputs and output in HOST memory: points_affine (n x 16
  * uint32), scalars (n x 8 uint32) and out_jacobian (24 uint32), layouts as for
  * msm_g1_run.  The call queues, on `stream`, the upload of the scalars, the
  * MSM and the download of the result; the points are uploaded on one of the
@@ -161,7 +170,9 @@ int msm_g1_run_batch(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint3
 int msm_g1_run_host(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *scalars, size_t n,
                     int window_c, uint32_t *out_jacobian, cudaStream_t stream);
 
-/* out_i = [k_i]G for the generator G = (1, 2), as affine Montgomery points
+/* Workload builder: the pages' "independent points" (PR #23736, section
+ * "Change (correct, landed)", which replaced an arithmetic progression of G).
+ * out_i = [k_i]G for the generator G = (1, 2), as affine Montgomery points
  * (n x 16 uint32, infinity as (0, 0)).  scalars: device, n x 8 uint32, any
  * 256-bit value.  A utility for building workloads P_i = [r_i]G on the device;
  * it is not part of the MSM.  Asynchronous on stream. */
@@ -191,14 +202,18 @@ int msm_g1_mul_generator(msm_g1_ctx *ctx, const uint32_t *scalars, size_t n, uin
 int msm_g1_run_noalloc(const uint32_t *points_affine, const uint32_t *scalars, size_t n, int window_c,
                        uint32_t *out_jacobian, cudaStream_t stream);
 
-/* Release the context's scratch (synchronises the context's device first).  NULL is a no-op. */
+/* No page counterpart.  Release the context's scratch (synchronises the context's device first).
+ * NULL is a no-op. */
 void msm_g1_destroy(msm_g1_ctx *ctx);
 
-/* Set / read a tunable (MSM_G1_PARAM_*).  Takes effect on the next run. */
+/* The pages' MsmConfig runtime knobs (PR #23738, section "What landed here").
+ * Set / read a tunable (MSM_G1_PARAM_*).  Takes effect on the next run. */
 int msm_g1_set_param(msm_g1_ctx *ctx, int key, int value);
 int msm_g1_get_param(const msm_g1_ctx *ctx, int key, int *value);
 
-/* With MSM_G1_PARAM_TIMING = 1: wait for the last run and copy up to nphase
+/* The pages' per-phase GPU times (the "stream_walker" phase beside the wall
+ * time: PR #23736, section "Real-hardware results").
+ * With MSM_G1_PARAM_TIMING = 1: wait for the last run and copy up to nphase
  * phase durations in milliseconds (decompose+histogram, scan, scatter,
  * accumulate level 0, accumulate levels >= 1, bucket reduction, window
  * combination) into ms.  Returns the number of phases written.  Timing runs
@@ -206,7 +221,9 @@ int msm_g1_get_param(const msm_g1_ctx *ctx, int key, int *value);
  * phases of different window groups overlap on the context's own streams. */
 int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
 
-/* Counters of the last run (waits for it): out[0] = bucket entries (non-zero
+/* The pages count inversions as total additions / S (PR #23736, section
+ * "Change (correct, landed)"); these are the counters behind such figures.
+ * Counters of the last run (waits for it): out[0] = bucket entries (non-zero
  * digits), out[1] = non-empty buckets, out[2] = largest bucket; with
  * MSM_G1_PARAM_STATS = 1 also out[3] = affine additions performed by the
  * accumulation, out[4] = field inversions it performed, out[5] = tree levels
@@ -217,7 +234,10 @@ int msm_g1_last_phase_ms(msm_g1_ctx *ctx, float *ms, int nphase);
  * Returns the number of counters written (at most nout, at most 11). */
 int msm_g1_last_stats(msm_g1_ctx *ctx, uint64_t *out, int nout);
 
-/* Host-only helpers (no device work). */
+/* Host-only helpers (no device work).  The window c is the pages' (c = 13 at
+ * n = 2^16: PR #23520 "cache dx + idx in ba_fused_super pref_scratch", section
+ * "Measurements"); the scratch size is their estimateMem (same page, section
+ * "Summary"); strerror has no page counterpart. */
 int msm_g1_window_count(int c);                      /* ceil(255 / c): signed windows for scalars reduced mod r
                                                         (without the GLV split; with it, ceil(128 / c)) */
 int msm_g1_auto_window(size_t n);                    /* the window the library picks for window_c = 0 */

@@ -49,6 +49,27 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 #define MSM_G1_TEST_JAC_DBL5_COOP 10 /* five doublings in a row ([32] a) by the window combination's chain */
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
+/* The residue-number-system chains of the window combination (one warp per
+ * element).  Field values are positional Montgomery form (8 words), points
+ * positional Jacobian (24 words), as in msm_g1_test_fq / msm_g1_test_g1.
+ *   RNS_MUL       out = a * b, through the RNS (must equal MSM_G1_TEST_FQ_MUL)
+ *   RNS_SQR_CHAIN out = a^(2^arg) by arg squarings in the RNS
+ *   RNS_DBL_N     out = 2^arg a (a finite, or infinity passed through)
+ *   RNS_ADD       out = a + b (finite); when a = +-b the chain reports equal x
+ *                 instead: out[0] = 0xffffffff, the rest 0
+ *   RNS_HORNER    a holds arg window sums per element (24 words each, window
+ *                 0 first); out = sum_w 2^(13 w) T_w by Horner's rule
+ *   RNS_IS_ZERO   a holds an integer below arg * p (8 words); out[i] = 1 if it
+ *                 is a multiple of p, else 0 (one word per element) */
+#define MSM_G1_TEST_RNS_MUL 0
+#define MSM_G1_TEST_RNS_SQR_CHAIN 1
+#define MSM_G1_TEST_RNS_DBL_N 2
+#define MSM_G1_TEST_RNS_ADD 3
+#define MSM_G1_TEST_RNS_HORNER 4
+#define MSM_G1_TEST_RNS_IS_ZERO 5
+int msm_g1_test_rns(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, int arg,
+                    cudaStream_t stream);
+
 /* Batched affine addition, the accumulation's inner step: out_i = a_i + b_i
  * for affine a, b (16 uint32 each), with one field inversion shared by each
  * run of batch_s consecutive pairs (batch_s as MSM_G1_PARAM_BATCH_S).

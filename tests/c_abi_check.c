@@ -18,7 +18,7 @@ int main(void) {
         (any_fn)msm_g1_window_count,    (any_fn)msm_g1_auto_window,    (any_fn)msm_g1_scratch_bytes,
         (any_fn)msm_g1_strerror,        (any_fn)msm_g1_test_fq,        (any_fn)msm_g1_test_g1,
         (any_fn)msm_g1_test_batch_add,  (any_fn)msm_g1_test_digits,    (any_fn)msm_g1_test_glv_split,
-        (any_fn)msm_g1_glv_constants,   (any_fn)msm_g1_debug_read,
+        (any_fn)msm_g1_glv_constants,   (any_fn)msm_g1_debug_read,     (any_fn)msm_g1_test_rns,
     };
     for (size_t i = 0; i < sizeof(entry) / sizeof(entry[0]); i++)
         if (!entry[i]) return 2;

@@ -392,6 +392,29 @@ def test_same_point_same_digit(n):
     assert oracle.words_to_point(got) == pyref.mul(31337 * n % pyref.R, pyref.G)
 
 
+@pytest.mark.parametrize("n,c,finish_t", [(20000, 13, 0), (20000, 10, 1), (70000, 13, 8)])
+def test_equal_scalars_fill_one_bucket_per_window(n, c, finish_t):
+    """All scalars equal: every window puts all n (or 2n) terms into one
+    bucket, far deeper than the tree levels launched one by one, so the
+    deep-level launch sums it (MSM = k sum_i P_i)."""
+    r, _ = synth.uniform_workload(n, 2024 + c)
+    pts = points_from_r(r)
+    kv = 0x1234567890ABCDEF1234567890ABCDEF1234567890ABCDEF1234567890ABCDE % pyref.R
+    k = oracle.ints_to_limbs([kv] * n)
+    cx = ctx(n, 16)
+    cx.set_param(gm.PARAM_FINISH, finish_t)
+    cx.set_param(gm.PARAM_STATS, 1)
+    try:
+        got = run_gpu(pts, k, c, max_n=n, max_c=16)
+        levels = cx.stats()["levels"]
+    finally:
+        cx.set_param(gm.PARAM_FINISH, 0)
+        cx.set_param(gm.PARAM_STATS, 0)
+    assert np.array_equal(got, oracle.closed_form(r, k))
+    if finish_t == 1:
+        assert levels >= 14  # the deep levels did the work (log2 n of them)
+
+
 def test_opposite_points_cancel():
     r = [11 + i for i in range(200)] + [pyref.R - 11 - i for i in range(200)]
     k = oracle.ints_to_limbs([5 + (i % 200) for i in range(400)])
