@@ -141,7 +141,7 @@ def parse():
     ap.add_argument("--c", type=int, default=0, help="override the window size")
     ap.add_argument("--batch-s", type=int, default=0,
                     help="additions per thread batch: 1..64, 0 = the library's choice (64)")
-    ap.add_argument("--tpb", type=int, default=128)
+    ap.add_argument("--tpb", type=int, default=0, help="threads per accumulation block (0 = the library's choice)")
     ap.add_argument("--place", type=int, default=0, choices=[0, 1, 2],
                     help="prefix products of a batch: 0 thread-local (device memory), 1 shared memory, 2 registers")
     ap.add_argument("--grid", type=int, default=0, help="most blocks per accumulation launch (0 = automatic)")
@@ -643,6 +643,7 @@ def run_gpu(args, cfg):
     per_config = None
     if K == 1 and not args.no_per_config:
         per_config = {}
+        pc_sampler = ClockSampler(uuid) if rank == 0 else None
         for name in PER_CONFIG:
             if name == args.config:
                 continue
@@ -655,6 +656,11 @@ def run_gpu(args, cfg):
             per_config[name] = r2
             del x2
             torch.cuda.empty_cache()
+        if pc_sampler:
+            # the larger configurations run back to back on a GPU already warm from
+            # the headline: their own clock record (a 2^20 MSM measured first in a
+            # fresh process ran 3.44 ms, measured after another context 3.53-3.58 ms)
+            per_config["clocks"] = pc_sampler.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -675,10 +681,10 @@ def run_gpu(args, cfg):
             "vs_baseline": (rec["points_per_s"] / (n / (PAGES_MS_LOGN16 / 1e3))) if n == (1 << 16) and K == 1
             else None,
             "dtype": "u32", "data": "synthetic",
-            "config": {"workload": "BN254 G1 MSM %sn=%d c=%d S=%s tpb=%d%s, %s points [r_i]G and scalars, seed %d"
-                                   % ("%d fused x " % K if K > 1 else "", n, c, args.batch_s or "auto", args.tpb,
+            "config": {"workload": "BN254 G1 MSM %sn=%d c=%d S=%s tpb=%s%s, %s points [r_i]G and scalars, seed %d"
+                                   % ("%d fused x " % K if K > 1 else "", n, c, args.batch_s or "auto", args.tpb or "auto",
                                       " GLV" if args.glv else "", cfg["kind"], cfg["seed"]),
-                       "n": n, "c": c, "S": args.batch_s or "auto", "tpb": args.tpb, "kind": cfg["kind"],
+                       "n": n, "c": c, "S": args.batch_s or "auto", "tpb": args.tpb or "auto", "kind": cfg["kind"],
                        "glv": args.glv, "batch": K, "finish_t": args.finish or "auto", "groups": args.groups,
                        "placement": ("local", "shared", "registers")[args.place], "grid": args.grid or "auto",
                        "msms_per_step": reps * K,

@@ -763,7 +763,13 @@ static int dense_levels(uint64_t terms_pw, uint32_t B, uint32_t finish_t) {
     return l - 1 < 1 ? 1 : l - 1;
 }
 
-// Window groups (top windows first) and their pair-list layout.
+// Window groups (top windows first) and their pair-list layout.  Two groups
+// (small MSMs) split unevenly: the top group takes about a quarter of the
+// windows, floor((W + 2) / 4).  Its sums then exist earlier, and the
+// doublings that must follow them -- about all the bits below the top window --
+// start earlier, while the larger lower group's own Horner chain is shorter
+// than that (GB300, n = 2^16, W = 10: top 3 0.790 ms, even split 0.810, top 2
+// 0.817; n = 2^10, W = 16: top 4 0.450, 5 0.452, 6 0.456, even 0.457).
 static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_t* total) {
     PairLayout lay;
     memset(&lay, 0, sizeof(lay));
@@ -771,10 +777,11 @@ static PairLayout make_layout(uint64_t n, int W, uint32_t B, int groups, uint64_
     lay.groups = groups;
     lay.B = B;
     const int per = (W + groups - 1) / groups;
+    const int top = groups == 2 ? std::max(1, (W + 2) / 4) : per;
     uint64_t base = 0;
     for (int j = 0; j < groups; j++) {
-        lay.w_hi[j] = std::max(0, W - j * per);
-        lay.w_lo[j] = std::max(0, W - (j + 1) * per);
+        lay.w_hi[j] = std::max(0, j == 0 ? W : W - top - (j - 1) * per);
+        lay.w_lo[j] = std::max(0, W - top - j * per);
         if (j == groups - 1) lay.w_lo[j] = 0;
         const uint64_t nw = (uint64_t)(lay.w_hi[j] - lay.w_lo[j]);
         const uint64_t nbj = nw * B;
@@ -973,7 +980,7 @@ int msm_g1_create_batch(msm_g1_ctx** out, size_t max_n, int max_c, int max_batch
     }
     layout(c, s, true);
     c->batch_s = 0;
-    c->tpb = 128;
+    c->tpb = 0;
     c->timing = 0;
     c->glv = 1;
     c->resident[0] = accum_resident_threads(64);
@@ -1058,7 +1065,7 @@ int msm_g1_set_param(msm_g1_ctx* c, int key, int value) {
             c->batch_s = value;
             return MSM_G1_OK;
         case MSM_G1_PARAM_TPB:
-            if (value != 64 && value != 128 && value != 256) return MSM_G1_ERR_INVALID_ARG;
+            if (value != 0 && value != 64 && value != 128 && value != 256) return MSM_G1_ERR_INVALID_ARG;
             c->tpb = value;
             return MSM_G1_OK;
         case MSM_G1_PARAM_TIMING:
@@ -1167,6 +1174,10 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     }
     const int stats = c->stats;
     int launches = 0;
+    // threads per accumulation block: automatic (0) takes 256 from 2^19 points
+    // (GB300: n = 2^20 3.474 -> 3.430 ms, 2^22 11.14 -> 10.95 ms) and 128 below
+    // (n = 2^16: 0.882 against 0.927 ms at 256)
+    const int tpb = c->tpb ? c->tpb : (n >= ((size_t)1 << 19) ? 256 : 128);
     // Points side: upload (host-buffer entry) and phi need only the points and
     // run on the side stream beside the sort, which needs only the scalars;
     // level 0 waits for them.  With phase timing (or without context streams)
@@ -1252,7 +1263,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     }
     mark(3);
     // the groups share the GPU in the pipelined schedule: size each grid for a share of it
-    Resident resident = c->resident[c->tpb == 64 ? 0 : c->tpb == 128 ? 1 : 2];
+    Resident resident = c->resident[tpb == 64 ? 0 : tpb == 128 ? 1 : 2];
     if (pipelined) {
         resident.narrow /= 2;
         resident.wide /= 2;
@@ -1260,7 +1271,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     const ReducePlan rp = reduce_plan(B);
     const uint32_t L = rp.L, G = rp.G;
     if (rp.jobs > MAX_REDUCE_JOBS) return MSM_G1_ERR_INVALID_ARG;  // unreachable for c <= 20
-    const AccumKnobs knobs{c->batch_s, c->tpb, c->acc_place, c->grid};
+    const AccumKnobs knobs{c->batch_s, tpb, c->acc_place, c->grid};
     c->last_finish_t = lay.finish_t;
     c->last_chunk_len = L;
     c->last_groups = (uint32_t)lay.groups;

@@ -63,12 +63,14 @@ extern "C" {
 #define MSM_G1_PARAM_BATCH_S 1 /* most additions a thread batches under one inversion: 1, 2, 4, 8, 16, 32, 64,
                                   or 0 = automatic (default, 64).  The pages' walkerS, additions per inversion
                                   (PR #23738 "stream-walker S-sweep", section "What landed here") */
-#define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256 (default 128).
-                                  The pages' walkerTpb (same section) */
+#define MSM_G1_PARAM_TPB 2     /* threads per block of the accumulation kernels: 64, 128, 256, or 0 =
+                                  automatic (default: 256 from 2^19 points, 128 below).  The pages' walkerTpb
+                                  (same section) */
 #define MSM_G1_PARAM_TIMING 3  /* 1: record CUDA events between phases (default 0) */
 #define MSM_G1_PARAM_STATS 4   /* 1: count additions and inversions on the device (default 0) */
 #define MSM_G1_PARAM_GROUPS 5  /* window groups pipelined over the context's streams: 1..4, 0 = automatic
-                                  (default: 2, and 3 from 2^19 points) */
+                                  (default: 2, and 3 from 2^19 points); of two groups the top one takes
+                                  floor((W + 2) / 4) of the W windows, otherwise they split evenly */
 #define MSM_G1_PARAM_FINISH 6  /* buckets with at most T items leave the affine tree and are summed in
                                   Jacobian coordinates: T = 1..64, 1 = never, 0 = automatic (default) */
 #define MSM_G1_PARAM_GLV 7     /* 1: split every scalar by the curve endomorphism (default), 0: plain windows */
