@@ -28,6 +28,7 @@
 #pragma once
 #include <stdint.h>
 
+#include "divstep_table.cuh"
 #include "fq.cuh"
 
 namespace inv {
@@ -79,6 +80,73 @@ __device__ __forceinline__ int32_t divsteps30(int32_t delta, uint32_t f, uint32_
     q_out = q;
     r_out = r;
     return delta;
+}
+
+// The same 30 divsteps with seven lookups of four steps each in the block's
+// copy of kDivTab (divstep_table.cuh, written by gen_divsteps.py), then two
+// single steps.  A lookup reads the 2x2 matrix B of four steps from delta and
+// the low four bits of f and g, advances f and g by B / 16 on their low words
+// and accumulates the batch matrix as B times it; four single steps cost a
+// chain of about 30 dependent instructions, a lookup a shared-memory load and
+// a few.  tab_sh: shared-memory address of the table (__cvta_generic_to_shared).
+__device__ __forceinline__ int32_t divsteps30_tab(int32_t delta, uint32_t f, uint32_t g, int32_t& u_out,
+                                                  int32_t& v_out, int32_t& q_out, int32_t& r_out, uint32_t tab_sh) {
+    int32_t u = 1, v = 0, q = 0, r = 1;
+#pragma unroll
+    for (int i = 0; i < 7; i++) {
+        const int32_t ds = min(max(delta, -4), 4) + 4;
+        const uint32_t idx = ((uint32_t)ds * 8u + ((f >> 1) & 7u)) * 16u + (g & 15u);
+        uint32_t e;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(e) : "r"(tab_sh + 4u * idx));
+        const int32_t bu = ((int32_t)(e << 26)) >> 26;
+        const int32_t bv = ((int32_t)(e << 20)) >> 26;
+        const int32_t bq = ((int32_t)(e << 14)) >> 26;
+        const int32_t br = ((int32_t)(e << 8)) >> 26;
+        const int32_t neg = -(int32_t)((e >> 24) & 1u);
+        const int32_t t = ((int32_t)(e << 2)) >> 27;
+        delta = ((delta ^ neg) - neg) + t;
+        const uint32_t fn = ((uint32_t)bu * f + (uint32_t)bv * g) >> 4;
+        const uint32_t gn = ((uint32_t)bq * f + (uint32_t)br * g) >> 4;
+        f = fn;
+        g = gn;
+        const int32_t un = bu * u + bv * q, vn = bu * v + bv * r;
+        const int32_t qn = bq * u + br * q, rn = bq * v + br * r;
+        u = un;
+        v = vn;
+        q = qn;
+        r = rn;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; i++) {  // steps 29 and 30, as in divsteps30
+        int32_t c1 = (-delta) >> 31;
+        int32_t c2 = -(int32_t)(g & 1u);
+        int32_t x = ((int32_t)f ^ c1) - c1;
+        int32_t y = (u ^ c1) - c1;
+        int32_t z = (v ^ c1) - c1;
+        g += (uint32_t)(x & c2);
+        q += y & c2;
+        r += z & c2;
+        c1 &= c2;
+        delta = (delta ^ c1) - c1 + 1;
+        f += g & (uint32_t)c1;
+        u += q & c1;
+        v += r & c1;
+        g >>= 1;
+        u <<= 1;
+        v <<= 1;
+    }
+    u_out = u;
+    v_out = v;
+    q_out = q;
+    r_out = r;
+    return delta;
+}
+
+// A block's copy of the divstep table in shared memory; every thread of the
+// block calls this before any of them may use the table, and a barrier
+// follows before the first lookup.
+__device__ __forceinline__ void load_divtab(uint32_t* tab) {
+    for (int i = threadIdx.x; i < kDivTabEntries; i += blockDim.x) tab[i] = __ldg(kDivTab + i);
 }
 
 // (f, g) := (u f + v g, q f + r g) / 2^30 (exact)
@@ -178,7 +246,9 @@ __device__ __forceinline__ void add_p_masked(s9& a, int32_t mask) {
 }
 
 // x~ (Montgomery form of x, < p) -> Montgomery form of x^-1; 0 -> 0.
-static __device__ __noinline__ fq::fe inv_safegcd(fq::fe xm) {
+// tab_sh: shared-memory address of the block's divstep table, or 0 for the
+// plain divstep loop (paths without the table in shared memory).
+static __device__ __noinline__ fq::fe inv_safegcd_impl(fq::fe xm, uint32_t tab_sh) {
     s9 f, g, d, e;
 #pragma unroll
     for (int i = 0; i < 9; i++) f.v[i] = p30(i);
@@ -194,8 +264,8 @@ static __device__ __noinline__ fq::fe inv_safegcd(fq::fe xm) {
 #pragma unroll 1
     for (int b = 0; b < BATCHES; b++) {
         int32_t u, v, q, r;
-        delta = divsteps30(delta, (uint32_t)f.v[0] | ((uint32_t)f.v[1] << 30),
-                           (uint32_t)g.v[0] | ((uint32_t)g.v[1] << 30), u, v, q, r);
+        const uint32_t fl = (uint32_t)f.v[0] | ((uint32_t)f.v[1] << 30), gl = (uint32_t)g.v[0] | ((uint32_t)g.v[1] << 30);
+        delta = tab_sh ? divsteps30_tab(delta, fl, gl, u, v, q, r, tab_sh) : divsteps30(delta, fl, gl, u, v, q, r);
         update_fg(f, g, u, v, q, r);
         update_de(d, e, u, v, q, r);
         // once g = 0 everywhere in the warp, further divsteps leave f and d unchanged
@@ -218,6 +288,12 @@ static __device__ __noinline__ fq::fe inv_safegcd(fq::fe xm) {
 #pragma unroll
     for (int i = 0; i < 9; i++) d.v[i] = (d.v[i] & keep) | (t.v[i] & ~keep);
     return to_fe(d);
+}
+
+__device__ __forceinline__ fq::fe inv_safegcd(fq::fe xm) { return inv_safegcd_impl(xm, 0u); }
+// the same with the block's table (tab: a shared-memory array filled by load_divtab)
+__device__ __forceinline__ fq::fe inv_safegcd_tab(fq::fe xm, const uint32_t* tab) {
+    return inv_safegcd_impl(xm, (uint32_t)__cvta_generic_to_shared(tab));
 }
 
 }  // namespace inv

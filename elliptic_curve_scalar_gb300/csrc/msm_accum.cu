@@ -108,6 +108,9 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     // narrow launches (one pair per thread) keep per-thread inversions: the
     // block's shared one would add warp 0's group products to their latency
     const bool share = chunk >= 2;
+    __shared__ uint32_t divtab[inv::kDivTabEntries];
+    inv::load_divtab(divtab);
+    __syncthreads();
     if (!share && count == 0) return;
     __shared__ uint32_t sh[8 * 256];
     extern __shared__ uint32_t pre_sh[];  // prefix products with PLACE_SHARED
@@ -133,7 +136,7 @@ __device__ __forceinline__ void accum_level0(LEVEL0_PARAMS) {
     }
     // the backward multiplications inlined in both builds of level 0 (n = 2^16,
     // natural build: 131 -> 127 us); the tree's narrow levels keep them called
-    int adds = batch_pairs<S, true, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh);
+    int adds = batch_pairs<S, true, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh, divtab);
     if (stats) warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
 }
 
@@ -252,6 +255,9 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     if ((uint64_t)blockIdx.x * blockDim.x * chunk >= cnt) return;
     const int count = i0 < cnt ? (int)min(chunk, (uint64_t)cnt - i0) : 0;
     const bool share = chunk >= 2;  // as in accum_level0
+    __shared__ uint32_t divtab[inv::kDivTabEntries];
+    inv::load_divtab(divtab);
+    __syncthreads();
     if (!share && count == 0) return;
     __shared__ uint32_t sh[8 * 256];
     extern __shared__ uint32_t pre_sh[];
@@ -265,7 +271,7 @@ __device__ __forceinline__ void accum_list(uint32_t* __restrict__ items, const u
     } else {
         for (int k = 0; k < count; k++) src.qi[k] = lst[i0 + k];
     }
-    int adds = batch_pairs<S, WIDE, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh);
+    int adds = batch_pairs<S, WIDE, PLACE>(src, count, inv_kind, share ? sh : nullptr, pre_sh, divtab);
     if (stats) {
         warp_stats(ctl, adds, share ? threadIdx.x < 32 : 1);
         if (threadIdx.x == 0) atomicMax(&ctl->levels, (uint32_t)level + 1);
@@ -300,6 +306,9 @@ __global__ void __launch_bounds__(256) k_accum_deep(uint32_t* __restrict__ items
                                                     PairLayout lay, ctl_t* ctl, int grp, int first, int stats,
                                                     int inv_kind) {
     __shared__ uint32_t sh[8 * 256];
+    __shared__ uint32_t divtab[inv::kDivTabEntries];
+    inv::load_divtab(divtab);
+    __syncthreads();
     int adds = 0, invs = 0;
     for (int level = first; level < MAX_LEVELS; level++) {
         const uint32_t cnt = ctl->pair_count[grp][level];
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(256) k_accum_deep(uint32_t* __restrict__ items
             src.half = 1u << (level - 1);
             for (int k = 0; k < count; k++) src.qi[k] = list[i0 + k];
             // every thread of the block takes part in the shared inversion
-            adds += batch_pairs<S, false>(src, count, inv_kind, sh);
+            adds += batch_pairs<S, false>(src, count, inv_kind, sh, nullptr, divtab);
             invs += threadIdx.x < 32;
             __syncthreads();  // the next round reuses sh; the next level reads these items
         }

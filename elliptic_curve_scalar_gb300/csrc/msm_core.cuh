@@ -220,7 +220,7 @@ __device__ __forceinline__ fe sh_load(const uint32_t* sh, int i) {
     return a;
 }
 
-__device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_kind) {
+__device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_kind, const uint32_t* divtab) {
     const int tid = threadIdx.x, warp = tid >> 5, nw = blockDim.x >> 5;
     fe v = a;
     fe keep[3];  // this warp's values below each level it multiplied at (nw <= 8)
@@ -233,7 +233,7 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
             v = fq::mul(v, sh_load(sh, tid + 32 * s));
         }
     }
-    if (warp == 0) v = inv_kind ? fq::inv_fermat(v) : inv::inv_safegcd(v);
+    if (warp == 0) v = inv_kind ? fq::inv_fermat(v) : divtab ? inv::inv_safegcd_tab(v, divtab) : inv::inv_safegcd(v);
     for (int s = 1; s < nw; s <<= 1) {
         lv--;
         if (warp < s) {
@@ -313,9 +313,11 @@ struct PreStore<S, PLACE_SHARED> {
 // one inversion (block_inverse): then every thread of the block must call,
 // those without pairs with count = 0.  pre_sh is the block's prefix-product
 // area for PLACE_SHARED (S x 8 x blockDim.x words), unused otherwise.
+// divtab: the block's shared-memory copy of the divstep table (inv.cuh,
+// load_divtab), or null for the plain divstep loop.
 template <int S, bool INLINE_BACK, int PLACE = PLACE_LOCAL, class Src>
 __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0, uint32_t* sh = nullptr,
-                                           uint32_t* pre_sh = nullptr) {
+                                           uint32_t* pre_sh = nullptr, const uint32_t* divtab = nullptr) {
     PreStore<S, PLACE> pre;
     if constexpr (PLACE == PLACE_SHARED) pre.base = pre_sh;
     fe acc = fq::one();
@@ -339,7 +341,8 @@ __device__ __forceinline__ int batch_pairs(Src& src, int count, int inv_kind = 0
 #pragma unroll 1
         for (int k = 0; k < count; k++) forward(k);
     }
-    fe inv = sh ? block_inverse(acc, sh, inv_kind) : inv_kind ? fq::inv_fermat(acc) : inv::inv_safegcd(acc);
+    fe inv = sh ? block_inverse(acc, sh, inv_kind, divtab)
+                : inv_kind ? fq::inv_fermat(acc) : divtab ? inv::inv_safegcd_tab(acc, divtab) : inv::inv_safegcd(acc);
     auto backward = [&](int k) {
         aff p = src.p(k);
         bool hq = src.has_q(k);

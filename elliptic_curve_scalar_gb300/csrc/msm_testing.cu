@@ -15,6 +15,9 @@ using g1::jac;
 namespace {
 
 __global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n) {
+    __shared__ uint32_t divtab[inv::kDivTabEntries];
+    inv::load_divtab(divtab);
+    __syncthreads();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     fe x = fq::load(a + 8 * i);
@@ -26,6 +29,7 @@ __global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t
         case MSM_G1_TEST_FQ_SUB: r = fq::sub(x, fq::load(b + 8 * i)); break;
         case MSM_G1_TEST_FQ_NEG: r = fq::neg(x); break;
         case MSM_G1_TEST_FQ_INV: r = inv::inv_safegcd(x); break;
+        case MSM_G1_TEST_FQ_INV_TABLE: r = inv::inv_safegcd_tab(x, divtab); break;
         default: r = fq::inv_fermat(x); break;
     }
     fq::store(out + 8 * i, r);
@@ -179,7 +183,7 @@ bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV_FERMAT) return MSM_G1_ERR_INVALID_ARG;
+    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV_TABLE) return MSM_G1_ERR_INVALID_ARG;
     bool needs_b = op == MSM_G1_TEST_FQ_MUL || op == MSM_G1_TEST_FQ_ADD || op == MSM_G1_TEST_FQ_SUB;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;

@@ -27,6 +27,8 @@ extern "C" {
 #define MSM_G1_TEST_FQ_NEG 4 /* out = -a              */
 #define MSM_G1_TEST_FQ_INV 5 /* out = a^-1 (0 -> 0), safegcd divsteps (the MSM's inversion) */
 #define MSM_G1_TEST_FQ_INV_FERMAT 6 /* out = a^(p-2) by square and multiply */
+#define MSM_G1_TEST_FQ_INV_TABLE 7 /* out = a^-1 (0 -> 0), safegcd with four divsteps per table lookup (the
+                                      accumulation kernels' inversion) */
 int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* Point operations.  JAC_* take and return Jacobian points (24 uint32),

@@ -23,7 +23,7 @@ def _field_inputs(n, seed):
     return vals
 
 
-@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv", "inv_fermat"])
+@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv", "inv_fermat", "inv_table"])
 def test_fq_ops(op):
     n = 4099  # several blocks and a ragged tail
     a = _field_inputs(n, 1)
