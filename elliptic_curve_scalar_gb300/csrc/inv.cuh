@@ -290,6 +290,84 @@ static __device__ __noinline__ fq::fe inv_safegcd_impl(fq::fe xm, uint32_t tab_s
     return to_fe(d);
 }
 
+// One pass of 32 inversions shared by two warps of a block (both call this,
+// converged; blockDim.x >= 64).  Lane i of warp 0 holds the value xm to invert
+// and runs the divsteps and the update of f and g -- the chain the next batch
+// waits for -- and hands each batch's transition matrix to lane i of warp 1
+// through shared memory; warp 1 applies it to the cofactors d and e, one batch
+// behind, which takes their 54 limb products off warp 0's path.  The two warps
+// meet at a named barrier (id 1, 64 threads) once per batch; the matrices
+// alternate between two buffers, so warp 0 rewrites a buffer only after warp 1
+// has passed the next meeting and is done with it.  mat: 2 x 6 x 32 words of
+// shared memory (u, v, q, r, the sign of f, the end flag).  The inverse is
+// returned in warp 1 (lane i: the inverse of warp 0's lane-i value); warp 0's
+// return value is unspecified.  tab_sh: the block's divstep table.
+__device__ __forceinline__ fq::fe inv_safegcd_pair(const fq::fe& xm, uint32_t* mat, uint32_t tab_sh) {
+    const int lane = threadIdx.x & 31;
+    const bool lead = (threadIdx.x >> 5) == 0;
+    const int32_t K[9] = {0x138afa89, 0x0cb3f16d, 0x04501fbf, 0x39c64475, 0x017ff6b5,
+                          0x2c7bfc29, 0x0351f47a, 0x27dc72ae, 0x6d8};  // R^2 mod p
+    s9 a, b;  // warp 0: f, g; warp 1: d, e
+    if (lead) {
+        const s9 g0 = from_fe(xm);
+#pragma unroll
+        for (int i = 0; i < 9; i++) {
+            a.v[i] = p30(i);
+            b.v[i] = g0.v[i];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 9; i++) {
+            a.v[i] = 0;
+            b.v[i] = K[i];
+        }
+    }
+    int32_t delta = 1, fneg = 0;
+#pragma unroll 1
+    for (int bt = 0; bt < BATCHES; bt++) {
+        uint32_t* m = mat + (bt & 1) * 6 * 32 + lane;
+        bool fin;
+        if (lead) {
+            int32_t u, v, q, r;
+            const uint32_t fl = (uint32_t)a.v[0] | ((uint32_t)a.v[1] << 30);
+            const uint32_t gl = (uint32_t)b.v[0] | ((uint32_t)b.v[1] << 30);
+            delta = divsteps30_tab(delta, fl, gl, u, v, q, r, tab_sh);
+            m[0] = (uint32_t)u;
+            m[32] = (uint32_t)v;
+            m[64] = (uint32_t)q;
+            m[96] = (uint32_t)r;
+            update_fg(a, b, u, v, q, r);
+            const int32_t gz = b.v[0] | b.v[1] | b.v[2] | b.v[3] | b.v[4] | b.v[5] | b.v[6] | b.v[7] | b.v[8];
+            fin = __all_sync(0xffffffffu, gz == 0);  // g = 0 in every lane: f and d are final
+            m[128] = (uint32_t)(a.v[8] >> 31);
+            m[160] = fin;
+            asm volatile("bar.sync 1, 64;" ::: "memory");
+        } else {
+            asm volatile("bar.sync 1, 64;" ::: "memory");
+            const int32_t u = (int32_t)m[0], v = (int32_t)m[32], q = (int32_t)m[64], r = (int32_t)m[96];
+            fneg = (int32_t)m[128];
+            fin = m[160] != 0;
+            update_de(a, b, u, v, q, r);
+        }
+        if (fin) break;
+    }
+    // warp 1: f = +-1, x^-1 = f d; bring d from (-2p, p) into [0, p)
+    s9& d = a;
+#pragma unroll
+    for (int i = 0; i < 9; i++) d.v[i] = (d.v[i] ^ fneg) - fneg;
+    normalise(d);
+    add_p_masked(d, d.v[8] >> 31);
+    add_p_masked(d, d.v[8] >> 31);
+    s9 t;
+#pragma unroll
+    for (int i = 0; i < 9; i++) t.v[i] = d.v[i] - p30(i);
+    normalise(t);
+    const int32_t keep = t.v[8] >> 31;
+#pragma unroll
+    for (int i = 0; i < 9; i++) d.v[i] = (d.v[i] & keep) | (t.v[i] & ~keep);
+    return to_fe(d);
+}
+
 __device__ __forceinline__ fq::fe inv_safegcd(fq::fe xm) { return inv_safegcd_impl(xm, 0u); }
 // the same with the block's table (tab: a shared-memory array filled by load_divtab)
 __device__ __forceinline__ fq::fe inv_safegcd_tab(fq::fe xm, const uint32_t* tab) {

@@ -233,7 +233,23 @@ __device__ __forceinline__ fe block_inverse(const fe& a, uint32_t* sh, int inv_k
             v = fq::mul(v, sh_load(sh, tid + 32 * s));
         }
     }
-    if (warp == 0) v = inv_kind ? fq::inv_fermat(v) : divtab ? inv::inv_safegcd_tab(v, divtab) : inv::inv_safegcd(v);
+    if (inv_kind == 0 && divtab && nw >= 2) {
+        // warps 0 and 1 share the pass (inv_safegcd_pair): warp 0 hands over
+        // its 32 values in slots 0..31 of sh (the tree keeps its own values in
+        // the slots of warps 1 and up) and warp 1 returns the inverses there
+        __shared__ uint32_t pair_mat[2 * 6 * 32];
+        if (warp == 0) sh_store(sh, tid, v);
+        __syncthreads();
+        if (warp < 2) {
+            const fe r = inv::inv_safegcd_pair(sh_load(sh, tid & 31), pair_mat,
+                                               (uint32_t)__cvta_generic_to_shared(divtab));
+            if (warp == 1) sh_store(sh, tid & 31, r);  // warp 0 read its slot before the first meeting
+        }
+        __syncthreads();
+        if (warp == 0) v = sh_load(sh, tid);
+    } else if (warp == 0) {
+        v = inv_kind ? fq::inv_fermat(v) : divtab ? inv::inv_safegcd_tab(v, divtab) : inv::inv_safegcd(v);
+    }
     for (int s = 1; s < nw; s <<= 1) {
         lv--;
         if (warp < s) {

@@ -19,6 +19,12 @@ __global__ void k_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t
     inv::load_divtab(divtab);
     __syncthreads();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (op == MSM_G1_TEST_FQ_INV_BLOCK) {  // the whole block takes part; past the end it inverts one
+        __shared__ uint32_t sh[8 * 128];
+        const fe r = msm::block_inverse(i < n ? fq::load(a + 8 * i) : fq::one(), sh, 0, divtab);
+        if (i < n) fq::store(out + 8 * i, r);
+        return;
+    }
     if (i >= n) return;
     fe x = fq::load(a + 8 * i);
     fe r;
@@ -183,7 +189,7 @@ bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV_TABLE) return MSM_G1_ERR_INVALID_ARG;
+    if (op < MSM_G1_TEST_FQ_MUL || op > MSM_G1_TEST_FQ_INV_BLOCK) return MSM_G1_ERR_INVALID_ARG;
     bool needs_b = op == MSM_G1_TEST_FQ_MUL || op == MSM_G1_TEST_FQ_ADD || op == MSM_G1_TEST_FQ_SUB;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;

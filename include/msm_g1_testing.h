@@ -28,7 +28,11 @@ extern "C" {
 #define MSM_G1_TEST_FQ_INV 5 /* out = a^-1 (0 -> 0), safegcd divsteps (the MSM's inversion) */
 #define MSM_G1_TEST_FQ_INV_FERMAT 6 /* out = a^(p-2) by square and multiply */
 #define MSM_G1_TEST_FQ_INV_TABLE 7 /* out = a^-1 (0 -> 0), safegcd with four divsteps per table lookup (the
-                                      accumulation kernels' inversion) */
+                                      accumulation kernels' per-thread inversion) */
+#define MSM_G1_TEST_FQ_INV_BLOCK 8 /* out = a^-1 for nonzero a: the block-shared inversion of the
+                                      accumulation kernels (128 values per block through one pass of 32
+                                      inversions shared by two warps); a zero makes its block's results
+                                      unspecified */
 int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* Point operations.  JAC_* take and return Jacobian points (24 uint32),

@@ -23,10 +23,12 @@ def _field_inputs(n, seed):
     return vals
 
 
-@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv", "inv_fermat", "inv_table"])
+@pytest.mark.parametrize("op", ["mul", "sqr", "add", "sub", "neg", "inv", "inv_fermat", "inv_table", "inv_block"])
 def test_fq_ops(op):
     n = 4099  # several blocks and a ragged tail
     a = _field_inputs(n, 1)
+    if op == "inv_block":  # the block's shared inversion takes nonzero values only
+        a = [x or 1 for x in a]
     b = list(reversed(_field_inputs(n, 2)))
     da = gm.to_device(ints_to_u32([mont(x) for x in a]))
     db = gm.to_device(ints_to_u32([mont(x) for x in b]))
