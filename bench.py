@@ -96,7 +96,7 @@ FR_R = 0x30644e72e131a029b85045b68181585d2833e84879b9709143e1f593f0000001
 # (bytes per MSM, per phase, per workload) for one build together with the
 # digest of these files at that build; the bench line reports the counters
 # only while the digest matches (any kernel change makes them stale).
-KERNEL_SOURCES = ("msm_g1.cu", "msm_accum.cu", "msm_internal.cuh", "msm_core.cuh", "g1_coop.cuh", "g1_rns.cuh",
+KERNEL_SOURCES = ("msm_g1.cu", "msm_accum.cu", "msm_internal.cuh", "msm_core.cuh", "g1_coop.cuh", "g1_proj.cuh",
                   "rns.cuh", "rns_consts.cuh", "g1.cuh", "glv.cuh", "inv.cuh", "divstep_table.cuh", "fq.cuh")
 
 

@@ -36,7 +36,7 @@
 
 #include "../../include/msm_g1.h"
 #include "g1_coop.cuh"
-#include "g1_rns.cuh"
+#include "g1_proj.cuh"
 #include "msm_internal.cuh"
 
 using fq::fe;
@@ -481,25 +481,28 @@ __global__ void __launch_bounds__(REDUCE_TPB) k_reduce_jobs(const uint32_t* __re
     if (threadIdx.x < 24) partials[((size_t)(w * jobs + job) * parts + part) * 24 + threadIdx.x] = sm[threadIdx.x];
 }
 
-// One warp per (window, job): the warp sums its job's partial sums and shifts
-// the result to its weight -- V_t by 2^t L (t + log2 L doublings), the sum of
-// C_j not at all -- so that the bits are weighted in parallel rather than by a
-// sequential Horner pass.  The doublings run in the residue number system
-// (g1_rns.cuh): a chain of them is latency-bound, and there a doubling costs
-// three RNS products (about 400 cycles each) instead of three positional ones
-// (about 870).  The shifted value replaces the job's first partial sum.
-__global__ void __launch_bounds__(32) k_reduce_shift(uint32_t* __restrict__ partials, int w_lo, uint32_t jobs,
+// One block of two warps per (window, job): it sums the job's partial sums
+// and shifts the result to its weight -- V_t by 2^t L (t + log2 L
+// doublings), the sum of C_j not at all -- so that the bits are weighted in
+// parallel rather than by a sequential Horner pass.  The doublings run on the
+// warp pair in residue arithmetic (g1_proj.cuh): a chain of them is
+// latency-bound, and there a doubling costs two rounds of RNS products
+// (about 400 cycles each, six products to a round) instead of three levels of
+// positional ones (about 870).  The shifted value replaces the job's first
+// partial sum.
+__global__ void __launch_bounds__(64) k_reduce_shift(uint32_t* __restrict__ partials, int w_lo, uint32_t jobs,
                                                      uint32_t parts, uint32_t log2L) {
+    __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
     const uint32_t w = (uint32_t)w_lo + blockIdx.x / jobs, q = blockIdx.x % jobs;
     uint32_t* src = partials + (size_t)(w * jobs + q) * parts * 24;
-    jac acc = g1::load_jac(src);
+    jac acc = g1::load_jac(src);  // both warps sum the parts (cooperatively within each)
     for (uint32_t p = 1; p < parts; p++) acc = g1c::add(acc, g1::load_jac(src + p * 24));
     const uint32_t shift = q == 0 ? 0 : q - 1 + log2L;
     if (shift) {
-        const rns::Ctx C = rns::make_ctx();
-        acc = g1r::dbl_n_positional(C, acc, (int)shift);
+        g1p::Pair P = g1p::make_pair(xch);
+        acc = g1p::dbl_n_positional(P, acc, (int)shift);
     }
-    __syncwarp();
+    __syncthreads();
     if (threadIdx.x == 0) g1::store_jac(src, acc);
 }
 
@@ -531,22 +534,24 @@ __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uin
 
 // ---------------------------------------------------------- 7. combination
 
-// One warp: Horner's rule over windows w_hi-1 .. w_lo (the chain of about
-// nbits - c doublings is the latency floor of the whole MSM), run in the
-// residue number system of g1_rns.cuh: three groups of ten lanes compute the
-// three products of each level of a doubling at once, each product a 32-bit
-// product per residue and two short base extensions, about 400 cycles where a
-// positional product is about 870.  The running value is carried between
-// window groups in acc; the first group starts from its top window, the last
-// writes out.
-__global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo, Windows L,
-                               uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int first, int last) {
-    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    const rns::Ctx C = rns::make_ctx();
+// Two warps: Horner's rule over windows w_hi-1 .. w_lo (the chain of about
+// nbits - c doublings is the latency floor of the whole MSM), run in residue
+// arithmetic and projective coordinates (g1_proj.cuh): six groups of ten
+// lanes compute a round of six products at once, each a 32-bit product per
+// residue and two short base extensions, about 400 cycles where a positional
+// product is about 870; a doubling is two rounds, an addition two.  The
+// running value is carried between window groups in acc; the first group
+// starts from its top window, the last writes out.
+__global__ void __launch_bounds__(64) k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo,
+                                                     Windows L, uint32_t* __restrict__ acc,
+                                                     uint32_t* __restrict__ out, int first, int last) {
+    __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
+    if (blockIdx.x != 0 || threadIdx.x >= 64) return;
+    g1p::Pair P = g1p::make_pair(xch);
     const jac q0 = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
     // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
-    const jac q = g1r::horner(
-        C, q0, first ? w_hi - 2 : w_hi - 1, w_lo, [&](int w) { return window_width(L, w); },
+    const jac q = g1p::horner(
+        P, q0, first ? w_hi - 2 : w_hi - 1, w_lo, [&](int w) { return window_width(L, w); },
         [&](int w) { return g1::load_jac(wsums + (size_t)w * 24); });
     if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
 }
@@ -557,10 +562,11 @@ __global__ void k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int
 // The shift depends on the earlier groups only, so it runs while the group is
 // still accumulating, and the group's sums leave only L's shorter chain and
 // one addition on the critical path.
-__global__ void k_combine_shift(uint32_t* __restrict__ acc, int bits) {
-    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    const rns::Ctx C = rns::make_ctx();
-    const jac q = g1r::dbl_n_positional(C, g1::load_jac(acc), bits);
+__global__ void __launch_bounds__(64) k_combine_shift(uint32_t* __restrict__ acc, int bits) {
+    __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
+    if (blockIdx.x != 0 || threadIdx.x >= 64) return;
+    g1p::Pair P = g1p::make_pair(xch);
+    const jac q = g1p::dbl_n_positional(P, g1::load_jac(acc), bits);
     if (threadIdx.x == 0) g1::store_jac(acc, q);
 }
 
@@ -572,12 +578,14 @@ __global__ void k_combine_join(uint32_t* __restrict__ acc, const uint32_t* __res
 }
 
 // Batches: one warp per MSM m, Horner's rule over its windows [m W, (m + 1) W).
-__global__ void k_combine_batch(const uint32_t* __restrict__ wsums, Windows L, uint32_t* __restrict__ out) {
+__global__ void __launch_bounds__(64) k_combine_batch(const uint32_t* __restrict__ wsums, Windows L,
+                                                      uint32_t* __restrict__ out) {
+    __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
     const uint32_t m = blockIdx.x;
     const uint32_t* ws = wsums + (size_t)m * L.W * 24;
-    const rns::Ctx C = rns::make_ctx();
-    const jac q = g1r::horner(
-        C, g1::load_jac(ws + (size_t)(L.W - 1) * 24), L.W - 2, 0, [&](int w) { return window_width(L, w); },
+    g1p::Pair P = g1p::make_pair(xch);
+    const jac q = g1p::horner(
+        P, g1::load_jac(ws + (size_t)(L.W - 1) * 24), L.W - 2, 0, [&](int w) { return window_width(L, w); },
         [&](int w) { return g1::load_jac(ws + (size_t)w * 24); });
     if (threadIdx.x == 0) g1::store_jac(out + (size_t)m * 24, q);
 }
@@ -1317,15 +1325,15 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
                                                                     lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
         k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, rp.tpb, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
                                                                           rp.parts, rp.m, c->partials);
-        k_reduce_shift<<<(unsigned)nw * rp.jobs, 32, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L));
+        k_reduce_shift<<<(unsigned)nw * rp.jobs, 64, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L));
         k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, c->wsums);
         launches += 4;
     };
     auto combine = [&](int j, cudaStream_t s) {
         if (count > 1)  // one warp per MSM of the batch
-            k_combine_batch<<<count, 32, 0, s>>>(c->wsums, win, out);
+            k_combine_batch<<<count, 64, 0, s>>>(c->wsums, win, out);
         else
-            k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
+            k_combine_part<<<1, 64, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
                                             j == lay.groups - 1);
         launches++;
     };
@@ -1365,9 +1373,9 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
             // the group's own Horner value on its stream; on the chain, the
             // running value shifted past the group's windows, then the join
             uint32_t* loc = c->qacc + 24 * (1 + j);
-            k_combine_part<<<1, 32, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, loc, out, 1, 0);
+            k_combine_part<<<1, 64, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, loc, out, 1, 0);
             CK(cudaEventRecord(c->ev_group[j], s));
-            k_combine_shift<<<1, 32, 0, c->chain_stream>>>(
+            k_combine_shift<<<1, 64, 0, c->chain_stream>>>(
                 c->qacc, window_offset(win, lay.w_hi[j]) - window_offset(win, lay.w_lo[j]));
             CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
             k_combine_join<<<1, 32, 0, c->chain_stream>>>(c->qacc, loc, out, j == lay.groups - 1);

@@ -5,7 +5,7 @@
 
 #include "../../include/msm_g1_testing.h"
 #include "g1_coop.cuh"
-#include "g1_rns.cuh"
+#include "g1_proj.cuh"
 #include "msm_core.cuh"
 
 using fq::fe;
@@ -76,11 +76,33 @@ __global__ void k_test_g1_coop(int op, const uint32_t* a, const uint32_t* b, uin
 }
 
 // The residue-number-system chains, one warp per element.
-__global__ void k_test_rns(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n, int arg) {
+__global__ void __launch_bounds__(64) k_test_rns(int op, const uint32_t* a, const uint32_t* b, uint32_t* out,
+                                                 size_t n, int arg) {
+    __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
     const size_t i = blockIdx.x;
     if (i >= n) return;
+    const bool t0 = threadIdx.x == 0;
+    if (op == MSM_G1_TEST_RNS_DBL_N || op == MSM_G1_TEST_RNS_ADD || op == MSM_G1_TEST_RNS_HORNER) {
+        // the two-warp chains of g1_proj.cuh
+        g1p::Pair P = g1p::make_pair(xch);
+        jac o;
+        if (op == MSM_G1_TEST_RNS_DBL_N) {
+            o = g1p::dbl_n_positional(P, g1::load_jac(a + 24 * i), arg);
+        } else if (op == MSM_G1_TEST_RNS_ADD) {
+            const g1p::rproj pa = g1p::to_proj(P, g1::load_jac(a + 24 * i));
+            const g1p::rproj pb = g1p::to_proj(P, g1::load_jac(b + 24 * i));
+            o = g1p::to_jac(P, g1p::add(P, pa, pb));
+        } else {
+            // a holds arg window sums (24 words each) for element i, top window last; width 13 each
+            const uint32_t* ws = a + (size_t)24 * arg * i;
+            o = g1p::horner(P, g1::load_jac(ws + 24 * (arg - 1)), arg - 2, 0, [](int) { return 13; },
+                            [&](int w) { return g1::load_jac(ws + 24 * w); });
+        }
+        if (t0) g1::store_jac(out + 24 * i, o);
+        return;
+    }
+    if (threadIdx.x >= 32) return;  // one warp
     const rns::Ctx C = rns::make_ctx();
-    const bool w0 = (threadIdx.x & 31) == 0;
     switch (op) {
         case MSM_G1_TEST_RNS_MUL:
         case MSM_G1_TEST_RNS_SQR_CHAIN: {
@@ -93,35 +115,12 @@ __global__ void k_test_rns(int op, const uint32_t* a, const uint32_t* b, uint32_
                 for (int k = 0; k < arg; k++) r = rns::mm(C, r, r);
             }
             const fq::fe o = rns::to_positional(C, rns::mm(C, r, rns::cout(C)));
-            if (w0) fq::store(out + 8 * i, o);
-            break;
-        }
-        case MSM_G1_TEST_RNS_DBL_N: {
-            const jac o = g1r::dbl_n_positional(C, g1::load_jac(a + 24 * i), arg);
-            if (w0) g1::store_jac(out + 24 * i, o);
-            break;
-        }
-        case MSM_G1_TEST_RNS_ADD: {
-            g1r::rjac s;
-            const bool ok = g1r::add(C, g1r::to_rns(C, g1::load_jac(a + 24 * i)), g1r::to_rns(C, g1::load_jac(b + 24 * i)), s);
-            const jac o = ok ? g1r::to_jac(C, s) : jac{fq::zero(), fq::zero(), fq::zero()};
-            if (w0) {
-                g1::store_jac(out + 24 * i, o);
-                if (!ok) out[24 * i] = 0xFFFFFFFFu;  // marks "equal x reported"
-            }
-            break;
-        }
-        case MSM_G1_TEST_RNS_HORNER: {
-            // a holds arg window sums (24 words each) for element i, top window last; width 13 each
-            const uint32_t* ws = a + (size_t)24 * arg * i;
-            const jac o = g1r::horner(C, g1::load_jac(ws + 24 * (arg - 1)), arg - 2, 0,
-                                      [](int) { return 13; }, [&](int w) { return g1::load_jac(ws + 24 * w); });
-            if (w0) g1::store_jac(out + 24 * i, o);
+            if (t0) fq::store(out + 8 * i, o);
             break;
         }
         default: {  // MSM_G1_TEST_RNS_IS_ZERO: the integer a (8 words) below arg * p, as residues
             const bool z = rns::is_zero(C, rns::residues(C, fq::load(a + 8 * i)), (uint32_t)arg);
-            if (w0) out[i] = z ? 1u : 0u;
+            if (t0) out[i] = z ? 1u : 0u;
             break;
         }
     }
@@ -220,7 +219,7 @@ extern "C" int msm_g1_test_rns(int op, const uint32_t* a, const uint32_t* b, uin
     const bool needs_b = op == MSM_G1_TEST_RNS_MUL || op == MSM_G1_TEST_RNS_ADD;
     if (!a || !out || !a16(a) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
     if (op == MSM_G1_TEST_RNS_HORNER && arg < 1) return MSM_G1_ERR_INVALID_ARG;
-    k_test_rns<<<(unsigned)n, 32, 0, st>>>(op, a, b, out, n, arg);
+    k_test_rns<<<(unsigned)n, 64, 0, st>>>(op, a, b, out, n, arg);
     return cudaGetLastError() == cudaSuccess ? MSM_G1_OK : MSM_G1_ERR_CUDA;
 }
 

@@ -55,14 +55,15 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 #define MSM_G1_TEST_JAC_DBL5_COOP 10 /* five doublings in a row ([32] a) by the window combination's chain */
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
-/* The residue-number-system chains of the window combination (one warp per
- * element).  Field values are positional Montgomery form (8 words), points
- * positional Jacobian (24 words), as in msm_g1_test_fq / msm_g1_test_g1.
+/* The residue-number-system arithmetic of the window combination and the
+ * bucket reduction's shifts (one block of two warps per element).  Field
+ * values are positional Montgomery form (8 words), points positional Jacobian
+ * (24 words), as in msm_g1_test_fq / msm_g1_test_g1.
  *   RNS_MUL       out = a * b, through the RNS (must equal MSM_G1_TEST_FQ_MUL)
  *   RNS_SQR_CHAIN out = a^(2^arg) by arg squarings in the RNS
- *   RNS_DBL_N     out = 2^arg a (a finite, or infinity passed through)
- *   RNS_ADD       out = a + b (finite); when a = +-b the chain reports equal x
- *                 instead: out[0] = 0xffffffff, the rest 0
+ *   RNS_DBL_N     out = 2^arg a, by the two-warp projective doubling chain
+ *   RNS_ADD       out = a + b by the complete projective addition (any a, b:
+ *                 infinity, a = b and a = -b included)
  *   RNS_HORNER    a holds arg window sums per element (24 words each, window
  *                 0 first); out = sum_w 2^(13 w) T_w by Horner's rule
  *   RNS_IS_ZERO   a holds an integer below arg * p (8 words); out[i] = 1 if it
