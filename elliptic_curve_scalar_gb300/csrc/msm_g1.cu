@@ -238,6 +238,50 @@ __global__ void k_scan_apply(const uint32_t* __restrict__ counts, uint32_t nb, c
     if (blockIdx.x == 0 && threadIdx.x == 0) offsets[nb] = ctl->total;
 }
 
+// Small bucket counts (nb <= SCAN_SMALL_MAX): the three passes above in one
+// block of 1024 threads -- thread t takes the run of buckets [t r, (t + 1) r),
+// r = ceil(nb / 1024) -- which saves two launches and their gaps (n = 2^10,
+// c = 8, 2048 buckets: scan phase 21 -> 11 us).  Runs of more than a few
+// buckets make the block's loads uncoalesced and the single SM the bottleneck
+// (n = 2^16, 40960 buckets: 27 -> 85 us), so larger counts keep three passes.
+constexpr uint32_t SCAN_SMALL_MAX = 1u << 12;
+__global__ void __launch_bounds__(1024) k_scan_small(const uint32_t* __restrict__ counts, uint32_t nb,
+                                                     uint32_t* __restrict__ offsets, uint32_t* __restrict__ cursor,
+                                                     uint32_t* __restrict__ entries, ctl_t* ctl) {
+    __shared__ uint32_t sm[33];
+    const uint32_t r = (nb + blockDim.x - 1) / blockDim.x;
+    const uint32_t b0 = threadIdx.x * r, b1 = min(b0 + r, nb);
+    uint32_t s = 0, mx = 0, ne = 0, ent = 0;
+    for (uint32_t g = b0; g < b1; g++) {
+        const uint32_t m = counts[g];
+        s += m + (m & 1);
+        mx = max(mx, m);
+        ne += m != 0;
+        ent += m;
+    }
+    uint32_t tot;
+    uint32_t off = block_excl_scan(s, sm, tot);
+    for (uint32_t g = b0; g < b1; g++) {
+        const uint32_t m = counts[g];
+        offsets[g] = off;
+        cursor[g] = off;
+        if (m & 1) entries[off + m] = HOLE;
+        off += m + (m & 1);
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    ne = __reduce_add_sync(0xffffffffu, ne);
+    ent = __reduce_add_sync(0xffffffffu, ent);
+    if ((threadIdx.x & 31) == 0) {
+        if (mx) atomicMax(&ctl->max_count, mx);
+        if (ne) atomicAdd(&ctl->nonempty, ne);
+        if (ent) atomicAdd(&ctl->entries, ent);
+    }
+    if (threadIdx.x == 0) {
+        offsets[nb] = tot;
+        ctl->total = tot;
+    }
+}
+
 // ------------------------------------------------------------- 3. scatter
 
 template <bool GLV>
@@ -691,11 +735,14 @@ struct msm_g1_ctx {
 static int window_count(int c) { return make_windows(c, PLAIN_BITS).W; }
 static int glv_window_count(int c) { return make_windows(c, GLV_BITS).W; }
 static uint32_t reduce_chunk_len(uint32_t B) {
-    // L = 4 keeps each chunk's running sum short (2L additions); from B = 2^13
+    // L = 4 (2 for windows of at most 8 bits) keeps each chunk's running sum
+    // short (2L additions); from B = 2^13
     // on, L grows so that G = B / L stays <= 2^12 and the subset sums of the
     // reduction ((1 + log2 G) G / 2 additions per window) stay small
     // (measured at n = 2^22, c = 16: G = 8192 made the subset sums 0.36 ms)
-    uint32_t L = 4;
+    // (n = 2^10, c = 8, B = 128: L = 2 made the MSM 0.400 -> 0.388 ms; at
+    // n = 2^16, c = 13, B = 4096 it was slower, 0.698 -> 0.729 ms)
+    uint32_t L = B <= 128 ? 2 : 4;
     while ((uint64_t)L * 4096 < B) L <<= 1;
     return std::min(L, B);
 }
@@ -1210,10 +1257,12 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     }
     CK(cudaMemsetAsync(c->ctl, 0, sizeof(ctl_t), st));
     CK(cudaMemsetAsync(c->counts, 0, 4ull * nb, st));
-    // large single MSMs with windows of at most 16 bits take the shared-memory
-    // sort (digit codes once, slices of one window per block); its code matrix
-    // lives in the item buffer, which the accumulation fills only afterwards
-    const bool slice_sort = c->slice_sort_ok && count == 1 && cw <= 16 && terms * W >= ((uint64_t)1 << 22);
+    // single MSMs with windows of at most 16 bits and 2^12 or more digits take
+    // the shared-memory sort (digit codes once, slices of one window per
+    // block); its code matrix lives in the item buffer, which the accumulation
+    // fills only afterwards (against the per-term digits and scatter: n = 2^16,
+    // c = 13, 0.698 -> 0.672 ms; n = 2^10, c = 8, 0.381 -> 0.359 ms)
+    const bool slice_sort = c->slice_sort_ok && count == 1 && cw <= 16 && terms * W >= ((uint64_t)1 << 12);
     const size_t tstride = (size_t)((terms + 3) & ~(uint64_t)3);
     uint32_t* codes = c->items;
     const uint32_t slices = (uint32_t)std::max(1, c->sms / W);
@@ -1232,9 +1281,15 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     }
     mark(1);
     const uint32_t ntiles = (nb + SCAN_TILE - 1) / SCAN_TILE;
-    k_scan_reduce<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->ctl);
-    k_scan_tiles<<<1, 1024, 0, st>>>(c->tile_sums, ntiles, c->ctl);
-    k_scan_apply<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->offsets, c->cursor, c->entries, c->ctl);
+    if (nb <= SCAN_SMALL_MAX) {
+        k_scan_small<<<1, 1024, 0, st>>>(c->counts, nb, c->offsets, c->cursor, c->entries, c->ctl);
+        launches -= 2;  // counted below as three
+    } else {
+        k_scan_reduce<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->ctl);
+        k_scan_tiles<<<1, 1024, 0, st>>>(c->tile_sums, ntiles, c->ctl);
+        k_scan_apply<<<ntiles, SCAN_TPB, 0, st>>>(c->counts, nb, c->tile_sums, c->offsets, c->cursor, c->entries,
+                                                  c->ctl);
+    }
     // Serial schedule (one stream, one window group) when phase timing is on --
     // the phase events then delimit whole phases -- or when the context has no
     // streams of its own; otherwise window groups are pipelined (below).

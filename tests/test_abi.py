@@ -99,6 +99,13 @@ def test_scratch_bytes(lib):
     assert lib.msm_g1_scratch_bytes(16, 0) == 0
 
 
+def test_noalloc_scratch_holds_its_documented_limit(lib):
+    """msm_g1_run_noalloc serves n <= 4096, c <= 10 from a fixed 8 MiB device
+    array; the sizing of a context for that limit must fit in it (a change of
+    the buffers' sizes that breaks this would make every such call fail)."""
+    assert 0 < lib.msm_g1_scratch_bytes(4096, 10) <= 8 << 20
+
+
 def test_strerror(lib):
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert lib.msm_g1_strerror(code)
