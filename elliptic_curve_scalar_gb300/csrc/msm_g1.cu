@@ -472,6 +472,66 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
     }
 }
 
+// Small MSMs (T >= 2, buckets that leave the tree with 2..T items are summed
+// in Jacobian form): the small-bucket finish and the chunk sums in one launch.
+// A group of W lanes per bucket (W = 1: one thread; W = 8: cooperative
+// additions) and L groups per chunk.  Group k forms its bucket's sum S_k (the
+// finish's mixed additions, the tree's single item, or infinity); the chunk's
+// groups then form the suffix sums U_k = S_k + ... + S_{L-1} by a scan across
+// groups (log2 L additions deep where one thread's running sum was L long)
+// and sum_k U_k by a tree (log2 L more), and group 0 stores
+// (sum_k U_k, U_0) -- what k_reduce_chunks stores -- with no jsum round trip
+// and one launch fewer.  A warp holds whole chunks (W L divides 32).
+__device__ __forceinline__ jac shfl_down_jac(const jac& p, int d) {
+    jac r;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        r.X.v[i] = __shfl_down_sync(0xffffffffu, p.X.v[i], d);
+        r.Y.v[i] = __shfl_down_sync(0xffffffffu, p.Y.v[i], d);
+        r.Z.v[i] = __shfl_down_sync(0xffffffffu, p.Z.v[i], d);
+    }
+    return r;
+}
+
+template <int W, int L>
+__global__ void k_finish_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ offsets,
+                                uint32_t finish_t, int w_lo, int nwin, uint32_t B, uint32_t G,
+                                uint32_t* __restrict__ chunks) {
+    static_assert(W * L <= 32 && 32 % (W * L) == 0, "a warp holds whole chunks");
+    const uint32_t gt = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t t = gt / (W * L), k = (gt / W) % L;
+    const bool live = t < (uint32_t)nwin * G;  // dead lanes add infinities and store nothing
+    const uint32_t w = (uint32_t)w_lo + t / G, j = t % G;
+    jac S = g1::jac_inf();
+    if (live) {
+        const uint32_t g = w * B + j * L + k;
+        const uint32_t og = offsets[g] >> 1, h = (offsets[g + 1] >> 1) - og;
+        const FinishPlan fp = finish_plan(h, finish_t);
+        if (fp.items >= 2) {
+            for (uint32_t i = 0; i < fp.items; i++)
+                S = g1c::add_mixed_w<W>(S, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
+        } else if (h) {
+            S = g1::to_jac(g1::load_aff(items + (size_t)og * 16));
+        }
+    }
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) {  // suffix sums
+        const jac o = shfl_down_jac(S, d * W);
+        if (k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
+    }
+    const jac run = S;
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) {  // their sum, into group 0
+        const jac o = shfl_down_jac(S, d * W);
+        if ((k & (2 * d - 1)) == 0 && k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
+    }
+    if (live && k == 0 && (threadIdx.x & (W - 1)) == 0) {
+        uint32_t* dst = chunks + ((size_t)w * G + j) * 48;
+        g1::store_jac(dst, S);
+        g1::store_jac(dst + 24, run);
+    }
+}
+
 // Sum of the n Jacobian points in sm[0 .. n) (n a power of two, n <= blockDim.x
 // <= 256, one point per thread slot); the result lands in sm[0].  Wide levels
 // use one thread per addition; once a level has at most one addition per warp,
@@ -1364,20 +1424,42 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     auto reduce = [&](int j, cudaStream_t s) {
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         const uint32_t threads = (uint32_t)nw * G;
-        if (lay.finish_t >= 2) {
+        // small MSMs: the finish and the chunk sums in one launch; cooperative
+        // groups while the buckets fill a quarter of the GPU at most
+        const bool coop = (uint64_t)nw * B * 8 <= c->resident[1].narrow / 4;
+        bool fused = lay.finish_t >= 2;
+        if (fused) {
+            const unsigned lanes = (unsigned)nw * B * (coop && L <= 4 ? 8 : 1);
+            const unsigned blocks = (lanes + 127) / 128;
+#define FC(WW, LL) k_finish_chunks<WW, LL><<<blocks, 128, 0, s>>>(c->items, c->offsets, lay.finish_t, lay.w_lo[j], \
+                                                                 nw, B, G, c->chunks)
+            if (coop && L == 1) FC(8, 1);
+            else if (coop && L == 2) FC(8, 2);
+            else if (coop && L == 4) FC(8, 4);
+            else if (L == 1) FC(1, 1);
+            else if (L == 2) FC(1, 2);
+            else if (L == 4) FC(1, 4);
+            else if (L == 8) FC(1, 8);
+            else fused = false;
+#undef FC
+        }
+        if (!fused && lay.finish_t >= 2) {
             launch_finish(c->items, c->offsets, (uint32_t)lay.w_lo[j] * B, (uint32_t)lay.w_hi[j] * B, lay.finish_t,
                           c->jsum, c->resident[1].narrow, s);
             launches++;
         }
-        // cooperative groups while the chunks fill a quarter of the GPU at most
-        // (n = 2^10, 512 chunks: reduction 0.22 -> 0.18 ms; at 2^16, with 5 k
-        // chunks per group, they made the MSM 2 % slower: idle lanes multiply)
-        if ((uint64_t)threads * 8 <= c->resident[1].narrow / 4)
-            k_reduce_chunks<8><<<(threads * 8 + 127) / 128, 128, 0, s>>>(
-                c->items, c->counts, c->offsets, c->jsum, lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
-        else
-            k_reduce_chunks<1><<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum,
-                                                                    lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
+        if (!fused) {
+            // cooperative groups while the chunks fill a quarter of the GPU at most
+            // (n = 2^10, 512 chunks: reduction 0.22 -> 0.18 ms; at 2^16, with 5 k
+            // chunks per group, they made the MSM 2 % slower: idle lanes multiply)
+            if ((uint64_t)threads * 8 <= c->resident[1].narrow / 4)
+                k_reduce_chunks<8><<<(threads * 8 + 127) / 128, 128, 0, s>>>(
+                    c->items, c->counts, c->offsets, c->jsum, lay.finish_t, lay.w_lo[j], nw, B, L, G, c->chunks);
+            else
+                k_reduce_chunks<1><<<(threads + 127) / 128, 128, 0, s>>>(c->items, c->counts, c->offsets, c->jsum,
+                                                                        lay.finish_t, lay.w_lo[j], nw, B, L, G,
+                                                                        c->chunks);
+        }
         k_reduce_jobs<<<(unsigned)nw * rp.jobs * rp.parts, rp.tpb, 0, s>>>(c->chunks, lay.w_lo[j], G, rp.jobs,
                                                                           rp.parts, rp.m, c->partials);
         k_reduce_shift<<<(unsigned)nw * rp.jobs, 64, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, ilog2(L));
