@@ -227,26 +227,71 @@ __device__ __forceinline__ g1::jac to_jac(Pair& P, const rproj& q) {
     return fq::is_zero(r.Z) ? g1::jac_inf() : r;
 }
 
-// 2^n t for a positional Jacobian t (any point, n >= 0), positional out
-__device__ __forceinline__ g1::jac dbl_n_positional(Pair& P, const g1::jac& t, int n) {
-    if (n <= 0 || fq::is_zero(t.Z)) return t;
-    rproj q = to_proj(P, t);
+// Projective positional form, for values that pass between kernels: (X, Y, Z)
+// canonical in Montgomery form (fq.cuh), 24 words, the identity (0, 1, 0).
+struct ppos {
+    fq::fe X, Y, Z;
+};
+__device__ __forceinline__ ppos load_ppos(const uint32_t* p) { return ppos{fq::load(p), fq::load(p + 8), fq::load(p + 16)}; }
+__device__ __forceinline__ void store_ppos(uint32_t* p, const ppos& q) {
+    fq::store(p, q.X);
+    fq::store(p + 8, q.Y);
+    fq::store(p + 16, q.Z);
+}
+
+// Two positional projective points into RNS form in one round.
+__device__ __forceinline__ void from_ppos2(Pair& P, const ppos& a, const ppos& b, rproj& ra, rproj& rb) {
+    const Ctx& C = P.C;
+    const rv cin = rns::cin(C);
+    rv x[6], y[6], p[6];
+    x[0] = rns::residues(C, a.X);
+    x[1] = rns::residues(C, a.Y);
+    x[2] = rns::residues(C, a.Z);
+    x[3] = rns::residues(C, b.X);
+    x[4] = rns::residues(C, b.Y);
+    x[5] = rns::residues(C, b.Z);
+#pragma unroll
+    for (int i = 0; i < 6; i++) y[i] = cin;
+    mm6(P, x, y, p);
+    ra = rproj{p[0], p[1], p[2]};
+    rb = rproj{p[3], p[4], p[5]};
+}
+__device__ __forceinline__ rproj from_ppos(Pair& P, const ppos& a) {
+    rproj r, unused;
+    from_ppos2(P, a, a, r, unused);
+    return r;
+}
+// one round and three conversions to positional form (coordinates below 40 p)
+__device__ __forceinline__ ppos to_ppos(Pair& P, const rproj& q) {
+    const Ctx& C = P.C;
+    const rv cout = rns::cout(C);
+    rv x[6], y[6], p[6];
+    x[0] = q.X;
+    x[1] = q.Y;
+    x[2] = q.Z;
+#pragma unroll
+    for (int i = 3; i < 6; i++) x[i] = q.X;
+#pragma unroll
+    for (int i = 0; i < 6; i++) y[i] = cout;
+    mm6(P, x, y, p);
+    return ppos{rns::to_positional(C, p[0]), rns::to_positional(C, p[1]), rns::to_positional(C, p[2])};
+}
+
+// q doubled n times
+__device__ __forceinline__ rproj dbl_n(Pair& P, rproj q, int n) {
     Side idle;
     idle.stage = 4;
     for (int i = 0; i < n; i++) q = dbl(P, q, idle);
-    return to_jac(P, q);
+    return q;
 }
 
 // Horner's rule over the window sums load(w_from) .. load(w_lo) (positional
-// Jacobian), from q0: q = 2^width(w) q + T_w for w = w_from down to w_lo.
+// Jacobian), from q: q = 2^width(w) q + T_w for w = w_from down to w_lo.
 // Each T_w is brought into projective RNS form in the spare slots of the
 // doublings before it (two doublings take the four steps; what a narrower
-// window leaves runs in rounds of its own).  Every lane returns the same
-// canonical result.
+// window leaves runs in rounds of its own).
 template <class Width, class Load>
-__device__ __forceinline__ g1::jac horner(Pair& P, const g1::jac& q0, int w_from, int w_lo, Width&& width,
-                                          Load&& load) {
-    rproj q = to_proj(P, q0);
+__device__ __forceinline__ rproj horner_proj(Pair& P, rproj q, int w_from, int w_lo, Width&& width, Load&& load) {
     for (int w = w_from; w >= w_lo; w--) {
         Side s;
         s.start(P.C, load(w));
@@ -254,7 +299,21 @@ __device__ __forceinline__ g1::jac horner(Pair& P, const g1::jac& q0, int w_from
         for (int i = 0; i < n; i++) q = dbl(P, q, s);
         q = add(P, q, finish(P, s));
     }
-    return to_jac(P, q);
+    return q;
+}
+
+// The same from a positional Jacobian q0 to a positional Jacobian result
+// (every lane the same, canonical).
+template <class Width, class Load>
+__device__ __forceinline__ g1::jac horner(Pair& P, const g1::jac& q0, int w_from, int w_lo, Width&& width,
+                                          Load&& load) {
+    return to_jac(P, horner_proj(P, to_proj(P, q0), w_from, w_lo, width, load));
+}
+
+// 2^n t for a positional Jacobian t (any point, n >= 0), positional out
+__device__ __forceinline__ g1::jac dbl_n_positional(Pair& P, const g1::jac& t, int n) {
+    if (n <= 0 || fq::is_zero(t.Z)) return t;
+    return to_jac(P, dbl_n(P, to_proj(P, t), n));
 }
 
 }  // namespace g1p

@@ -643,42 +643,57 @@ __global__ void __launch_bounds__(32 * MAX_REDUCE_JOBS) k_reduce_final(const uin
 // arithmetic and projective coordinates (g1_proj.cuh): six groups of ten
 // lanes compute a round of six products at once, each a 32-bit product per
 // residue and two short base extensions, about 400 cycles where a positional
-// product is about 870; a doubling is two rounds, an addition two.  The
-// running value is carried between window groups in acc; the first group
-// starts from its top window, the last writes out.
+// product is about 870; a doubling is two rounds, an addition two.  The first
+// group starts from its top window, a later one from the running value in acc
+// (projective positional form, g1p::ppos); the result is doubled shift_after
+// more times (a later group's bits, in the pipelined schedule) and goes to
+// acc, or, from the last group, to out as a Jacobian point.
 __global__ void __launch_bounds__(64) k_combine_part(const uint32_t* __restrict__ wsums, int w_hi, int w_lo,
                                                      Windows L, uint32_t* __restrict__ acc,
-                                                     uint32_t* __restrict__ out, int first, int last) {
+                                                     uint32_t* __restrict__ out, int first, int last,
+                                                     int shift_after) {
     __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
     if (blockIdx.x != 0 || threadIdx.x >= 64) return;
     g1p::Pair P = g1p::make_pair(xch);
-    const jac q0 = first ? g1::load_jac(wsums + (size_t)(w_hi - 1) * 24) : g1::load_jac(acc);
+    const g1p::rproj q0 = first ? g1p::to_proj(P, g1::load_jac(wsums + (size_t)(w_hi - 1) * 24))
+                                : g1p::from_ppos(P, g1p::load_ppos(acc));
     // Q = 2^(off_{w+1} - off_w) Q + T_w, the shift being window w's width
-    const jac q = g1p::horner(
+    g1p::rproj q = g1p::horner_proj(
         P, q0, first ? w_hi - 2 : w_hi - 1, w_lo, [&](int w) { return window_width(L, w); },
         [&](int w) { return g1::load_jac(wsums + (size_t)w * 24); });
-    if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
+    q = g1p::dbl_n(P, q, shift_after);
+    if (last) {
+        const jac r = g1p::to_jac(P, q);
+        if (threadIdx.x == 0) g1::store_jac(out, r);
+    } else {
+        const g1p::ppos r = g1p::to_ppos(P, q);
+        if (threadIdx.x == 0) g1p::store_ppos(acc, r);
+    }
 }
 
 // In the pipelined schedule a later group's windows w_lo .. w_hi-1 enter the
 // running value Q as Q' = 2^(off_hi - off_lo) Q + L, where L is the group's
-// own Horner value (k_combine_part with first = 1, on the group's stream).
-// The shift depends on the earlier groups only, so it runs while the group is
-// still accumulating, and the group's sums leave only L's shorter chain and
-// one addition on the critical path.
-__global__ void __launch_bounds__(64) k_combine_shift(uint32_t* __restrict__ acc, int bits) {
+// own Horner value (k_combine_part with first = 1 into loc, on the group's
+// stream).  The shift depends on the earlier groups only: the chain kernel
+// before this one applies it (shift_after) while the group still
+// accumulates, so the group's sums leave only L's shorter chain and this
+// addition on the critical path; the join then applies the next group's
+// shift.  acc and loc hold projective positional points.
+__global__ void __launch_bounds__(64) k_combine_join(uint32_t* __restrict__ acc, const uint32_t* __restrict__ loc,
+                                                     uint32_t* __restrict__ out, int last, int shift_after) {
     __shared__ __align__(16) uint32_t xch[g1p::kXchWords];
     if (blockIdx.x != 0 || threadIdx.x >= 64) return;
     g1p::Pair P = g1p::make_pair(xch);
-    const jac q = g1p::dbl_n_positional(P, g1::load_jac(acc), bits);
-    if (threadIdx.x == 0) g1::store_jac(acc, q);
-}
-
-__global__ void k_combine_join(uint32_t* __restrict__ acc, const uint32_t* __restrict__ loc,
-                               uint32_t* __restrict__ out, int last) {
-    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
-    jac q = g1c::add(g1::load_jac(acc), g1::load_jac(loc));
-    if (threadIdx.x == 0) g1::store_jac(last ? out : acc, q);
+    g1p::rproj a, b;
+    g1p::from_ppos2(P, g1p::load_ppos(acc), g1p::load_ppos(loc), a, b);
+    const g1p::rproj q = g1p::dbl_n(P, g1p::add(P, a, b), shift_after);
+    if (last) {
+        const jac r = g1p::to_jac(P, q);
+        if (threadIdx.x == 0) g1::store_jac(out, r);
+    } else {
+        const g1p::ppos r = g1p::to_ppos(P, q);
+        if (threadIdx.x == 0) g1p::store_ppos(acc, r);
+    }
 }
 
 // Batches: one warp per MSM m, Horner's rule over its windows [m W, (m + 1) W).
@@ -1466,12 +1481,15 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         k_reduce_final<<<nw, 32 * rp.jobs, 0, s>>>(c->partials, lay.w_lo[j], rp.jobs, rp.parts, c->wsums);
         launches += 4;
     };
-    auto combine = [&](int j, cudaStream_t s) {
-        if (count > 1)  // one warp per MSM of the batch
+    // the bits of window group j (the shift a later group's own Horner value
+    // needs before it joins the running value)
+    auto group_bits = [&](int j) { return window_offset(win, lay.w_hi[j]) - window_offset(win, lay.w_lo[j]); };
+    auto combine = [&](int j, cudaStream_t s, int shift_after) {
+        if (count > 1)  // one warp pair per MSM of the batch
             k_combine_batch<<<count, 64, 0, s>>>(c->wsums, win, out);
         else
             k_combine_part<<<1, 64, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, c->qacc, out, j == 0,
-                                            j == lay.groups - 1);
+                                            j == lay.groups - 1, shift_after);
         launches++;
     };
     if (!pipelined) {
@@ -1481,7 +1499,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
         mark(5);
         reduce(0, st);
         mark(6);
-        combine(0, st);
+        combine(0, st, 0);
         mark(7);
     } else {
         // Window groups, top windows first, each on its own accumulation
@@ -1501,22 +1519,23 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
             // 0.714 -> 0.675 ms, 2^16: 1.071 -> 1.048 ms); for larger MSMs, with
             // three groups, the group's own Horner chain on its low-priority
             // stream waited behind the accumulation (2^20: 3.84 -> 3.91 ms)
+            // (with the split, each chain kernel also shifts the running value
+            // past the next group's windows while that group accumulates)
+            const int shift_next = split_combine && j + 1 < lay.groups ? group_bits(j + 1) : 0;
             if (j == 0 || !split_combine) {
                 CK(cudaEventRecord(c->ev_group[j], s));
                 CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
-                combine(j, c->chain_stream);
+                combine(j, c->chain_stream, shift_next);
                 continue;
             }
-            // the group's own Horner value on its stream; on the chain, the
-            // running value shifted past the group's windows, then the join
+            // the group's own Horner value on its stream; on the chain the join
+            // with the running value, already shifted past the group's windows
             uint32_t* loc = c->qacc + 24 * (1 + j);
-            k_combine_part<<<1, 64, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, loc, out, 1, 0);
+            k_combine_part<<<1, 64, 0, s>>>(c->wsums, lay.w_hi[j], lay.w_lo[j], win, loc, out, 1, 0, 0);
             CK(cudaEventRecord(c->ev_group[j], s));
-            k_combine_shift<<<1, 64, 0, c->chain_stream>>>(
-                c->qacc, window_offset(win, lay.w_hi[j]) - window_offset(win, lay.w_lo[j]));
             CK(cudaStreamWaitEvent(c->chain_stream, c->ev_group[j], 0));
-            k_combine_join<<<1, 32, 0, c->chain_stream>>>(c->qacc, loc, out, j == lay.groups - 1);
-            launches += 3;
+            k_combine_join<<<1, 64, 0, c->chain_stream>>>(c->qacc, loc, out, j == lay.groups - 1, shift_next);
+            launches += 2;
         }
         CK(cudaEventRecord(c->ev_chain, c->chain_stream));
         CK(cudaStreamWaitEvent(st, c->ev_chain, 0));
