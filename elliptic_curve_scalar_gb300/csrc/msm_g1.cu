@@ -474,14 +474,16 @@ __global__ void k_reduce_chunks(const uint32_t* __restrict__ items, const uint32
 
 // Small MSMs (T >= 2, buckets that leave the tree with 2..T items are summed
 // in Jacobian form): the small-bucket finish and the chunk sums in one launch.
-// A group of W lanes per bucket (W = 1: one thread; W = 8: cooperative
-// additions) and L groups per chunk.  Group k forms its bucket's sum S_k (the
-// finish's mixed additions, the tree's single item, or infinity); the chunk's
-// groups then form the suffix sums U_k = S_k + ... + S_{L-1} by a scan across
-// groups (log2 L additions deep where one thread's running sum was L long)
-// and sum_k U_k by a tree (log2 L more), and group 0 stores
-// (sum_k U_k, U_0) -- what k_reduce_chunks stores -- with no jsum round trip
-// and one launch fewer.  A warp holds whole chunks (W L divides 32).
+// A group of W lanes per point operation (W = 1: one thread; W = 8:
+// cooperative additions), H groups per bucket and L buckets per chunk.  The
+// H groups of a bucket add its items i = r, r + H, ... (mixed additions) and
+// then each other's sums, so that a bucket's chain is about T / H + log2 H
+// additions long; group r = 0 then holds the bucket's sum S_k (or its single
+// tree item, or infinity).  The chunk's buckets form the suffix sums
+// U_k = S_k + ... + S_{L-1} by a scan (log2 L additions deep, where one
+// thread's running sum was L long) and sum_k U_k by a tree (log2 L more),
+// and bucket 0 stores (sum_k U_k, U_0) -- what k_reduce_chunks stores -- with
+// no Jacobian bucket sums going through memory.  A warp holds whole chunks.
 __device__ __forceinline__ jac shfl_down_jac(const jac& p, int d) {
     jac r;
 #pragma unroll
@@ -493,13 +495,13 @@ __device__ __forceinline__ jac shfl_down_jac(const jac& p, int d) {
     return r;
 }
 
-template <int W, int L>
+template <int W, int H, int L>
 __global__ void k_finish_chunks(const uint32_t* __restrict__ items, const uint32_t* __restrict__ offsets,
                                 uint32_t finish_t, int w_lo, int nwin, uint32_t B, uint32_t G,
                                 uint32_t* __restrict__ chunks) {
-    static_assert(W * L <= 32 && 32 % (W * L) == 0, "a warp holds whole chunks");
+    static_assert(W * H * L <= 32 && 32 % (W * H * L) == 0, "a warp holds whole chunks");
     const uint32_t gt = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t t = gt / (W * L), k = (gt / W) % L;
+    const uint32_t t = gt / (W * H * L), k = (gt / (W * H)) % L, r = (gt / W) % H;
     const bool live = t < (uint32_t)nwin * G;  // dead lanes add infinities and store nothing
     const uint32_t w = (uint32_t)w_lo + t / G, j = t % G;
     jac S = g1::jac_inf();
@@ -508,24 +510,29 @@ __global__ void k_finish_chunks(const uint32_t* __restrict__ items, const uint32
         const uint32_t og = offsets[g] >> 1, h = (offsets[g + 1] >> 1) - og;
         const FinishPlan fp = finish_plan(h, finish_t);
         if (fp.items >= 2) {
-            for (uint32_t i = 0; i < fp.items; i++)
+            for (uint32_t i = r; i < fp.items; i += H)
                 S = g1c::add_mixed_w<W>(S, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
-        } else if (h) {
+        } else if (h && r == 0) {
             S = g1::to_jac(g1::load_aff(items + (size_t)og * 16));
         }
     }
 #pragma unroll
-    for (int d = 1; d < L; d <<= 1) {  // suffix sums
+    for (int d = 1; d < H; d <<= 1) {  // the bucket's groups, into group 0
         const jac o = shfl_down_jac(S, d * W);
-        if (k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
+        if ((r & (2 * d - 1)) == 0 && r + d < (uint32_t)H) S = g1c::add_w<W>(S, o);
+    }
+#pragma unroll
+    for (int d = 1; d < L; d <<= 1) {  // suffix sums over the chunk's buckets
+        const jac o = shfl_down_jac(S, d * W * H);
+        if (r == 0 && k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
     }
     const jac run = S;
 #pragma unroll
-    for (int d = 1; d < L; d <<= 1) {  // their sum, into group 0
-        const jac o = shfl_down_jac(S, d * W);
-        if ((k & (2 * d - 1)) == 0 && k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
+    for (int d = 1; d < L; d <<= 1) {  // their sum, into bucket 0
+        const jac o = shfl_down_jac(S, d * W * H);
+        if (r == 0 && (k & (2 * d - 1)) == 0 && k + d < (uint32_t)L) S = g1c::add_w<W>(S, o);
     }
-    if (live && k == 0 && (threadIdx.x & (W - 1)) == 0) {
+    if (live && k == 0 && r == 0 && (threadIdx.x & (W - 1)) == 0) {
         uint32_t* dst = chunks + ((size_t)w * G + j) * 48;
         g1::store_jac(dst, S);
         g1::store_jac(dst + 24, run);
@@ -1439,18 +1446,23 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     auto reduce = [&](int j, cudaStream_t s) {
         const int nw = lay.w_hi[j] - lay.w_lo[j];
         const uint32_t threads = (uint32_t)nw * G;
-        // small MSMs: the finish and the chunk sums in one launch; cooperative
-        // groups while the buckets fill a quarter of the GPU at most
-        const bool coop = (uint64_t)nw * B * 8 <= c->resident[1].narrow / 4;
+        // small MSMs: the finish and the chunk sums in one launch.  While the
+        // buckets fill a quarter of the GPU at most, four threads share each
+        // bucket's chain (n = 2^10: 0.355 -> 0.349 ms; eight-lane cooperative
+        // additions on one chain took 0.355); above that the launch is bound by
+        // issue slots and one thread per bucket is fastest (n = 2^16: 0.650 ms,
+        // two threads 0.763, four 0.889).
+        const bool small = (uint64_t)nw * B * 8 <= c->resident[1].narrow / 4;
         bool fused = lay.finish_t >= 2;
         if (fused) {
-            const unsigned lanes = (unsigned)nw * B * (coop && L <= 4 ? 8 : 1);
+            const unsigned lanes = (unsigned)nw * B * (small ? 4 : 1);
             const unsigned blocks = (lanes + 127) / 128;
-#define FC(WW, LL) k_finish_chunks<WW, LL><<<blocks, 128, 0, s>>>(c->items, c->offsets, lay.finish_t, lay.w_lo[j], \
-                                                                 nw, B, G, c->chunks)
-            if (coop && L == 1) FC(8, 1);
-            else if (coop && L == 2) FC(8, 2);
-            else if (coop && L == 4) FC(8, 4);
+#define FC(HH, LL) k_finish_chunks<1, HH, LL><<<blocks, 128, 0, s>>>(c->items, c->offsets, lay.finish_t, \
+                                                                    lay.w_lo[j], nw, B, G, c->chunks)
+            if (small && L == 1) FC(4, 1);
+            else if (small && L == 2) FC(4, 2);
+            else if (small && L == 4) FC(4, 4);
+            else if (small && L == 8) FC(4, 8);
             else if (L == 1) FC(1, 1);
             else if (L == 2) FC(1, 2);
             else if (L == 4) FC(1, 4);
