@@ -82,7 +82,7 @@ IMAD_SLOTS_JDBL = 2 * IMAD_SLOTS_PER_FQ_MUL + 5 * IMAD_SLOTS_PER_FQ_SQR
 IMAD_PHASES = {
     "accum_l0": "k_accum_level0 (+ _wide)",
     "accum_tree": "k_accum_list (+ _wide), one launch per tree level",
-    "bucket_reduce": "k_finish, k_reduce_chunks, k_reduce_jobs, k_reduce_final",
+    "bucket_reduce": "k_finish_chunks (or k_finish + k_reduce_chunks), k_reduce_jobs, k_reduce_shift, k_reduce_final",
     "combine": "k_combine_part",
 }
 # the larger configurations measured into the line's per_config block
@@ -188,16 +188,22 @@ def workload(cfg):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_points_per_s(cfg, sample, threads=None):
-    """Time the CPU oracle (as it stands) on the first ``sample`` terms."""
+def oracle_points_per_s(cfg, sample, threads=None, min_seconds=0.0):
+    """Time the CPU oracle (as it stands) on the workload's first ``sample``
+    points, the whole MSM repeated until ``min_seconds`` have passed; returns
+    (points/s, seconds, threads, repetitions)."""
     import oracle
     r, k = workload(dict(cfg, n=sample))
     pts = oracle.generator_multiples(r, threads=threads)
     threads = threads or oracle.default_threads()
+    reps = 0
     t0 = time.perf_counter()
-    oracle.msm(pts, k, threads=threads)
-    dt = time.perf_counter() - t0
-    return sample / dt, dt, threads
+    while True:
+        oracle.msm(pts, k, threads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            return sample * reps / dt, dt, threads, reps
 
 
 def run_reference(args, cfg):
@@ -207,11 +213,11 @@ def run_reference(args, cfg):
             import torch.distributed as dist
             dist.destroy_process_group()
         return 0
-    sample = 8192
+    sample = min(8192, cfg["n"])
     vals, times = [], []
     threads = None
     for i in range(args.warmup + args.steps):
-        v, dt, threads = oracle_points_per_s(cfg, sample)
+        v, dt, threads, _ = oracle_points_per_s(cfg, sample)
         if i >= args.warmup:
             vals.append(v)
             times.append(dt)
@@ -221,10 +227,10 @@ def run_reference(args, cfg):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * statistics.mean(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u64", "data": "synthetic",
-        "config": {"workload": "BN254 G1 MSM %s, CPU oracle on the first %d terms per step" % (args.config, sample),
+        "config": {"workload": "BN254 G1 MSM %s, CPU oracle on the first %d points per step" % (args.config, sample),
                    "n": cfg["n"], "c": cfg["c"], "kind": cfg["kind"], "seed": cfg["seed"]},
         "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
-                         "sample": "first %d terms of the %s workload per step" % (sample, args.config)},
+                         "sample": "first %d points of the %s workload per step" % (sample, args.config)},
         "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -664,11 +670,14 @@ def run_gpu(args, cfg):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # a bounded sample: about 13 core-seconds of oracle work (0.8 s wall on 16 Grace cores)
-        sample = 65536
-        v, dt, threads = oracle_points_per_s(cfg, sample)
+        # a bounded sample: at most 2^16 of the workload's points (about 13
+        # core-seconds of oracle work, 0.8 s wall on 16 Grace cores), smaller
+        # workloads whole and repeated for half a second at least
+        sample = min(65536, cfg["n"])
+        v, dt, threads, reps = oracle_points_per_s(cfg, sample, min_seconds=0.5)
         cpu = {"value": v, "unit": "points/s", "cores": threads, "kind": "oracle",
-               "sample": "first %d terms of the %s workload (%.1f s wall)" % (sample, args.config, dt)}
+               "sample": "first %d points of the %s workload, %d MSM(s) (%.1f s wall)" % (sample, args.config,
+                                                                                    reps, dt)}
 
     if rank == 0:
         steps_msms = x["steps_msms"]
