@@ -94,22 +94,61 @@ FR_R = 0x30644e72e131a029b85045b68181585d2833e84879b9709143e1f593f0000001
 
 # The library's kernel sources.  profiles/traffic.json holds ncu DRAM counters
 # (bytes per MSM, per phase, per workload) for one build together with the
-# digest of these files at that build; the bench line reports the counters
-# only while the digest matches (any kernel change makes them stale).
+# digest of these files' code at that build; the bench line reports the
+# counters only while the digest matches (any code change makes them stale,
+# an edited comment does not).
 KERNEL_SOURCES = ("msm_g1.cu", "msm_accum.cu", "msm_internal.cuh", "msm_core.cuh", "g1_coop.cuh", "g1_proj.cuh",
                   "rns.cuh", "rns_consts.cuh", "g1.cuh", "glv.cuh", "inv.cuh", "divstep_table.cuh", "fq.cuh")
 
 
+def code_only(src):
+    """C/C++ source bytes without comments, whitespace runs collapsed to one
+    space (string and character literals kept as they are): what the compiler
+    sees, so that an edited comment leaves the digest below unchanged."""
+    out, i, n = bytearray(), 0, len(src)
+
+    def space():
+        if out and out[-1] != 0x20:
+            out.append(0x20)
+
+    while i < n:
+        c = src[i:i + 1]
+        if src.startswith(b"//", i):
+            j = src.find(b"\n", i)
+            i = n if j < 0 else j
+        elif src.startswith(b"/*", i):
+            j = src.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+            space()
+        elif c in (b'"', b"'"):
+            j = i + 1
+            while j < n and src[j:j + 1] != c:
+                j += 2 if src[j:j + 1] == b"\\" else 1
+            out += src[i:j + 1]
+            i = j + 1
+        elif c.isspace():
+            j = i
+            while j < n and src[j:j + 1].isspace():
+                j += 1
+            space()
+            i = j
+        else:
+            out += c
+            i += 1
+    return bytes(out).strip()
+
+
 def kernel_sources_digest(read=None):
-    """sha256 over KERNEL_SOURCES (name and contents of each, in order);
-    read(name) -> bytes supplies the contents (default: the working tree)."""
+    """sha256 over KERNEL_SOURCES (name and code of each, in order, comments
+    left out: code_only); read(name) -> bytes supplies the contents (default:
+    the working tree)."""
     if read is None:
         def read(name):
             with open(os.path.join(ROOT, "elliptic_curve_scalar_gb300", "csrc", name), "rb") as f:
                 return f.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        h.update(name.encode() + b"\0" + read(name) + b"\0")
+        h.update(name.encode() + b"\0" + code_only(read(name)) + b"\0")
     return h.hexdigest()
 
 

@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(64) k_combine_join(uint32_t* __restrict__ acc,
     }
 }
 
-// Batches: one warp per MSM m, Horner's rule over its windows [m W, (m + 1) W).
+// Batches: one warp pair per MSM m, Horner's rule over its windows [m W, (m + 1) W).
 __global__ void __launch_bounds__(64) k_combine_batch(const uint32_t* __restrict__ wsums, Windows L,
                                                       uint32_t* __restrict__ out) {
     __shared__ __align__(16) uint32_t xch[g1p::kXchWords];

@@ -148,7 +148,7 @@ int msm_g1_run(msm_g1_ctx *ctx, const uint32_t *points_affine, const uint32_t *s
  * terms, layouts as for msm_g1_run); offsets: HOST array of count + 1
  * nondecreasing term offsets with offsets[0] = 0 (empty MSMs give infinity).
  * The MSMs run fused -- one sort, one accumulation pass, one reduction over
- * the windows of all MSMs of a pass and one combination warp per MSM -- which
+ * the windows of all MSMs of a pass and one combination warp pair per MSM -- which
  * is what makes many small MSMs cheap; a batch larger than the context's
  * buffers is split into consecutive passes.  window_c applies to every MSM
  * (0: chosen for the largest one).  Each MSM must have at most max_n terms.

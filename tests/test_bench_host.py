@@ -45,6 +45,19 @@ def test_digest_follows_every_source():
         assert bench.kernel_sources_digest(lambda nm: changed[nm]) != d0
 
 
+def test_digest_ignores_comments_but_not_code():
+    src = b'int f(int x) { // doubles x\n  return 2 * x; /* block\n comment */ }\nconst char* s = "a // b";\n'
+    base = {name: src for name in bench.KERNEL_SOURCES}
+    d0 = bench.kernel_sources_digest(lambda name: base[name])
+    recommented = src.replace(b"doubles x", b"twice x").replace(b"block", b"a longer block")
+    respaced = src.replace(b"return 2 * x;", b"return   2 *  x;")
+    for other in (recommented, respaced):
+        assert bench.kernel_sources_digest(lambda nm: dict(base, **{"fq.cuh": other})[nm]) == d0
+    for other in (src.replace(b"2 * x", b"3 * x"), src.replace(b'"a // b"', b'"a / b"')):
+        assert bench.kernel_sources_digest(lambda nm: dict(base, **{"fq.cuh": other})[nm]) != d0
+    assert bench.code_only(b'x = 1; // y\n"//z" /* w */ q') == b'x = 1; "//z" q'
+
+
 def test_traffic_only_for_the_build_it_was_taken_on(tmp_path):
     prof = tmp_path / "traffic.json"
     prof.write_text(json.dumps({"bytes_per_msm": {"n2p16": {"accum_tree": 123}},
