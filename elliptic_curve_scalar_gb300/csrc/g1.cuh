@@ -80,6 +80,30 @@ __device__ __forceinline__ jac add_mixed(const jac& p, const aff& q) {
     return r;
 }
 
+// mmadd-2007-bl (affine + affine, Z1 = Z2 = 1): H = x2 - x1, HH = H^2,
+// I = 4HH, J = H I, r = 2(y2 - y1), V = x1 I, X3 = r^2 - J - 2V,
+// Y3 = r(V - X3) - 2 y1 J, Z3 = 2H: 4M + 2S where the mixed addition of the
+// second point onto the first takes 7M + 4S.
+__device__ __forceinline__ jac add_aff(const aff& p, const aff& q) {
+    if (is_inf(p)) return to_jac(q);
+    if (is_inf(q)) return to_jac(p);
+    fe H = fq::sub(q.x, p.x);
+    fe rr = fq::sub(q.y, p.y);
+    if (fq::is_zero(H)) {
+        if (fq::is_zero(rr)) return dbl(to_jac(p));
+        return jac_inf();
+    }
+    rr = fq::dbl(rr);
+    fe I = fq::dbl(fq::dbl(fq::sqr(H)));
+    fe J = fq::mul(H, I);
+    fe V = fq::mul(p.x, I);
+    jac r;
+    r.X = fq::sub(fq::sub(fq::sqr(rr), J), fq::dbl(V));
+    r.Y = fq::sub(fq::mul(rr, fq::sub(V, r.X)), fq::dbl(fq::mul(p.y, J)));
+    r.Z = fq::dbl(H);
+    return r;
+}
+
 // add-2007-bl (Jacobian + Jacobian): Z1Z1 = Z1^2, Z2Z2 = Z2^2, U1 = X1 Z2Z2,
 // U2 = X2 Z1Z1, S1 = Y1 Z2 Z2Z2, S2 = Y2 Z1 Z1Z1, H = U2 - U1, I = (2H)^2,
 // J = H I, r = 2(S2 - S1), V = U1 I, X3 = r^2 - J - 2V,

@@ -510,8 +510,15 @@ __global__ void k_finish_chunks(const uint32_t* __restrict__ items, const uint32
         const uint32_t og = offsets[g] >> 1, h = (offsets[g + 1] >> 1) - og;
         const FinishPlan fp = finish_plan(h, finish_t);
         if (fp.items >= 2) {
-            for (uint32_t i = r; i < fp.items; i += H)
-                S = g1c::add_mixed_w<W>(S, g1::load_aff(items + (size_t)(og + i * fp.stride) * 16));
+            auto item = [&](uint32_t i) { return g1::load_aff(items + (size_t)(og + i * fp.stride) * 16); };
+            uint32_t i = r;
+            if constexpr (W == 1) {  // the chain's first two items by the affine-affine addition
+                if (i + H < fp.items) {
+                    S = g1::add_aff(item(i), item(i + H));
+                    i += 2 * H;
+                }
+            }
+            for (; i < fp.items; i += H) S = g1c::add_mixed_w<W>(S, item(i));
         } else if (h && r == 0) {
             S = g1::to_jac(g1::load_aff(items + (size_t)og * 16));
         }

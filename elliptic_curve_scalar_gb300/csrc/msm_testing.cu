@@ -52,6 +52,9 @@ __global__ void k_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t
         case MSM_G1_TEST_JAC_MIXED:
             g1::store_jac(out + 24 * i, g1::add_mixed(g1::load_jac(a + 24 * i), g1::load_aff(b + 16 * i)));
             break;
+        case MSM_G1_TEST_AFF_ADD:
+            g1::store_jac(out + 24 * i, g1::add_aff(g1::load_aff(a + 16 * i), g1::load_aff(b + 16 * i)));
+            break;
         default: g1::store_aff(out + 16 * i, g1::to_aff(g1::load_jac(a + 24 * i))); break;
     }
 }
@@ -198,14 +201,14 @@ extern "C" int msm_g1_test_fq(int op, const uint32_t* a, const uint32_t* b, uint
 
 extern "C" int msm_g1_test_g1(int op, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t n,
                               cudaStream_t st) {
-    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_JAC_DBL5_COOP) return MSM_G1_ERR_INVALID_ARG;
+    if (op < MSM_G1_TEST_JAC_DBL || op > MSM_G1_TEST_AFF_ADD) return MSM_G1_ERR_INVALID_ARG;
     bool needs_b = op != MSM_G1_TEST_JAC_DBL && op != MSM_G1_TEST_TO_AFFINE && op != MSM_G1_TEST_JAC_DBL_COOP &&
                    op != MSM_G1_TEST_JAC_DBL_COOP8 && op != MSM_G1_TEST_JAC_DBL5_COOP;
     if (n == 0) return MSM_G1_OK;
     if (!a || !out || !a16(a) || !a16(out) || (needs_b && (!b || !a16(b)))) return MSM_G1_ERR_INVALID_ARG;
     if (op >= MSM_G1_TEST_JAC_DBL_COOP8 && op <= MSM_G1_TEST_JAC_MIXED_COOP8)
         k_test_g1_coop<8><<<(unsigned)((n * 8 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
-    else if (op >= MSM_G1_TEST_JAC_DBL_COOP)
+    else if (op >= MSM_G1_TEST_JAC_DBL_COOP && op <= MSM_G1_TEST_JAC_DBL5_COOP)
         k_test_g1_coop<32><<<(unsigned)((n * 32 + 127) / 128), 128, 0, st>>>(op, a, b, out, n);
     else
         k_test_g1<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(op, a, b, out, n);

@@ -49,7 +49,8 @@ STATS = ("entries", "nonempty_buckets", "max_bucket", "adds", "inversions", "lev
 
 TEST_FQ = {"mul": 0, "sqr": 1, "add": 2, "sub": 3, "neg": 4, "inv": 5, "inv_fermat": 6, "inv_table": 7, "inv_block": 8}
 TEST_G1 = {"jac_dbl": 0, "jac_add": 1, "jac_mixed": 2, "to_affine": 3, "jac_dbl_coop": 4, "jac_add_coop": 5,
-           "jac_mixed_coop": 6, "jac_dbl_coop8": 7, "jac_add_coop8": 8, "jac_mixed_coop8": 9, "jac_dbl5_coop": 10}
+           "jac_mixed_coop": 6, "jac_dbl_coop8": 7, "jac_add_coop8": 8, "jac_mixed_coop8": 9, "jac_dbl5_coop": 10,
+           "aff_add": 11}
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t

@@ -53,6 +53,7 @@ int msm_g1_test_fq(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, 
 #define MSM_G1_TEST_JAC_ADD_COOP8 8
 #define MSM_G1_TEST_JAC_MIXED_COOP8 9
 #define MSM_G1_TEST_JAC_DBL5_COOP 10 /* five doublings in a row ([32] a) by the window combination's chain */
+#define MSM_G1_TEST_AFF_ADD 11 /* a + b for affine a, b (16 words each) into Jacobian (the finish's first step) */
 int msm_g1_test_g1(int op, const uint32_t *a, const uint32_t *b, uint32_t *out, size_t n, cudaStream_t stream);
 
 /* The residue-number-system arithmetic of the window combination and the

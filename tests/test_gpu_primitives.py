@@ -82,6 +82,10 @@ def test_jacobian_ops():
     add8s = gm.to_host(gm.test_g1("jac_add_coop8", db, da))
     mix8 = gm.to_host(gm.test_g1("jac_mixed_coop8", da, dab))
     dbl5 = gm.to_host(gm.test_g1("jac_dbl5_coop", da))
+    # affine + affine (the finish's first step): a's affine words against b's
+    aa = gm.to_device(np.stack([point_to_aff_words(p) for p in a]))
+    affadd = gm.to_host(gm.test_g1("aff_add", aa, dab))
+    affdbl = gm.to_host(gm.test_g1("aff_add", aa, aa))
     for i, (p, q) in enumerate(zip(a, b)):
         assert jac_words_to_point(dbl[i]) == pyref.add(p, p), ("dbl", i)
         assert jac_words_to_point(add[i]) == pyref.add(p, q), ("add", i)
@@ -96,6 +100,8 @@ def test_jacobian_ops():
         assert jac_words_to_point(add8s[i]) == pyref.add(q, p), ("add_coop8 swapped", i)
         assert jac_words_to_point(mix8[i]) == pyref.add(p, q), ("mixed_coop8", i)
         assert jac_words_to_point(dbl5[i]) == pyref.mul(32, p), ("dbl5_coop", i)
+        assert jac_words_to_point(affadd[i]) == pyref.add(p, q), ("aff_add", i)
+        assert jac_words_to_point(affdbl[i]) == pyref.add(p, p), ("aff_add P+P", i)
         assert aff_words_to_point(aff[i]) == p, ("to_affine", i)
 
 
