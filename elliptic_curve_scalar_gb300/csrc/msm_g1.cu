@@ -884,10 +884,14 @@ static uint64_t level_cap(uint64_t h_ub, uint64_t nb, int l) {
 // (GB300 with the cooperative reduction: n = 2^16, T = 2 / 4 / 8 / 16: 0.912 /
 // 0.926 / 0.898 / 0.977 ms; 2^10, T = 4 / 8 / 16: 0.549 / 0.545 / 0.538 ms;
 // from 2^20 every T >= 2 was slower).
-static int auto_finish(uint64_t n, int W, uint64_t resident) {
+static int auto_finish(uint64_t n, int W, uint32_t B, uint64_t resident) {
     const uint64_t pairs1 = n * (uint64_t)W / 4;  // about the level-1 pairs
     if (pairs1 >= 8 * resident) return 1;
     if (pairs1 >= 2 * resident) return 8;
+    // buckets so few that four threads share each finish chain (k_finish_chunks):
+    // no tree level beyond level 0 (n = 2^10, c = 8: 0.341 ms at T = 16,
+    // 0.333 at T = 20 ... 48)
+    if ((uint64_t)W * B * 8 <= resident / 4) return 32;
     return 16;
 }
 
@@ -1393,7 +1397,7 @@ static int run_core(msm_g1_ctx* c, const uint32_t* points, const uint32_t* scala
     // per window bounds the entries of all of them together)
     const uint64_t terms_pw = (terms + count - 1) / count;
     PairLayout lay = make_layout(terms_pw, Wall, B, pipelined ? groups : 1, &pairs_total);
-    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, c->resident[1].narrow));
+    lay.finish_t = (uint32_t)(c->finish_t ? c->finish_t : auto_finish(terms, W, B, c->resident[1].narrow));
     if (pairs_total > c->cap_pairs) return MSM_G1_ERR_CAPACITY;
     launch_build_pairs(c->offsets, nb, c->pairs, lay, c->ctl, st);
     launches += 4;
