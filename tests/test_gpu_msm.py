@@ -180,6 +180,20 @@ def test_small_bucket_finish(mid_case, finish_t):
     assert np.array_equal(got, expect)
 
 
+@pytest.mark.parametrize("c,finish_t", [(8, 4), (8, 32), (16, 2), (16, 8)])
+def test_small_bucket_finish_chunk_lengths(mid_case, c, finish_t):
+    """The fused finish and chunk sums with chunks of two buckets (c = 8, four
+    threads per bucket's chain) and of eight (c = 16, one thread each)."""
+    pts, k, expect = mid_case
+    cx = ctx(20000, c)
+    cx.set_param(gm.PARAM_FINISH, finish_t)
+    try:
+        got = normalise(cx.run(gpu_points(pts), gpu_scalars(k), c))
+    finally:
+        cx.set_param(gm.PARAM_FINISH, 0)
+    assert np.array_equal(got, expect)
+
+
 def _host_inputs(pts, k, pin=True):
     p = torch.from_numpy(oracle.points_to_gpu_layout(pts).view(np.int32))
     s_ = torch.from_numpy(synth.scalars_to_u32(k).view(np.int32))
