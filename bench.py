@@ -704,7 +704,7 @@ def run_gpu(args, cfg):
         if pc_sampler:
             # the larger configurations run back to back on a GPU already warm from
             # the headline: their own clock record (a 2^20 MSM measured first in a
-            # fresh process ran 3.44 ms, measured after another context 3.53-3.58 ms)
+            # fresh process runs 3.39 ms, measured here after the headline 3.60 ms)
             per_config["clocks"] = pc_sampler.stop()
 
     cpu = None
